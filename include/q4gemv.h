@@ -1,0 +1,165 @@
+/*
+ * q4gemv.h -- C ABI of a GB300 (sm_103a) library of memory-bound decode GEMVs over 4-bit block-quantized
+ * weights.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers owned by the caller; the library never allocates, frees or keeps
+ *    them. Outputs must not overlap inputs.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream) and returns
+ *    as soon as the work is enqueued. Inputs must stay valid and unmodified until the work completes.
+ *  - Return value: Q4_OK (0) when the work was enqueued, otherwise a negative code; nothing is enqueued when
+ *    an argument is refused. The library refuses out-of-range arguments instead of clamping them.
+ *      Q4_EINVAL       null required pointer, a size <= 0, M outside 1..8, K not a multiple of the block
+ *                      size (32 for Q4, 256 for Q4_K), topk > E, eps negative or not finite
+ *      Q4_EALIGN       a pointer below the alignment stated for it
+ *      Q4_ECUDA        a CUDA call failed (launch error, no device, ...)
+ *      Q4_EUNSUPPORTED the current device is not sm_103, or the staged input (M*K*4 bytes, T*K*4 for MoE)
+ *                      does not fit in one CTA's shared memory next to the weight rings
+ *    q4_last_error() describes the most recent refusal or failure of the calling thread.
+ *  - Kernels never trap and contain no spin loops: each warp waits only for its own asynchronous copies.
+ *  - Inputs are fp32 vectors, outputs fp32. Weights are packed as described per format below; multi-byte
+ *    fields are little-endian.
+ *
+ * Formats
+ * -------
+ *  Q4 (planar; inferencelayer 0.2.13, src/bin/kernel_lab.rs, shader GEMV_F16S and its bindings
+ *  `scales`/`quants`): a row of K weights is K/32 blocks. qs is uint8[N][K/32][16] and d is
+ *  binary16[N][K/32] (raw bits in uint16). In block b, byte j holds weight 32b+j in its low nibble and
+ *  weight 32b+j+16 in its high nibble; the weight is (q - 8) * d[n][b].
+ *
+ *  Q4_K (trueno-gpu 0.4.11, src/kernels/quantize/fused.rs, FusedRmsNormQ4KGemvKernel phase 3): a row is
+ *  K/256 super-blocks of 144 bytes: binary16 d at byte 0, binary16 dmin at byte 2, 12 bytes of packed
+ *  6-bit scales/mins at 4..15 and 128 quant bytes at 16..143. Sub-block j (weights 32j..32j+31) has
+ *  scale sc and min m: for j < 4, sc = s[j] & 63 and m = s[j+4] & 63; for j >= 4,
+ *  sc = (s[j+4] & 15) | ((s[j-4] >> 6) << 4) and m = (s[j+4] >> 4) | ((s[j] >> 6) << 4). Weight e is in
+ *  quant byte 32*(e/64) + e%32, low nibble when e%64 < 32, else high nibble; its value is
+ *  d*sc*q - dmin*m.
+ *
+ * Numerics: products and sums run in fp32 (packed fp32x2 FMAs), so results differ from exact arithmetic by
+ * the order of summation; the library's tests hold every output within 1e-3 * sum_k |w_k||x_k| + 1e-5 of
+ * an fp64 reference. The dequant entry points are bit-exact.
+ */
+#ifndef Q4GEMV_H
+#define Q4GEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *q4_stream_t; /* the same type as cudaStream_t */
+
+enum {
+    Q4_OK = 0,
+    Q4_EINVAL = -1,
+    Q4_EALIGN = -2,
+    Q4_ECUDA = -3,
+    Q4_EUNSUPPORTED = -4
+};
+
+/* Fault bits reported by q4_device_faults. */
+enum {
+    Q4_FAULT_BAD_EXPERT = 4 /* moe_q4_gemv or moe_q4_pure_read saw an expert id outside [0, E) */
+};
+
+/*
+ * y[n] = sum_k W[n][k] * x[k], W in planar Q4 (see Formats).
+ * Source: inferencelayer kernel_lab.rs, shader GEMV_F16S (one column of its output).
+ *   y   float[N]          output                       (4-byte aligned)
+ *   qs  uint8[N][K/32][16] packed codes                (16-byte aligned)
+ *   d   uint16[N][K/32]   binary16 block scales        (2-byte aligned; 16-byte aligned and K % 256 == 0
+ *                                                       let the scales ride the bulk copies)
+ *   x   float[K]          input                        (16-byte aligned)
+ *   N >= 1; K >= 32 and K % 32 == 0.
+ */
+int q4_gemv(float *y, const uint8_t *qs, const uint16_t *d, const float *x, int N, int K, q4_stream_t stream);
+
+/*
+ * Y[m][n] = sum_k W[n][k] * X[m][k] for m < M, reading every weight byte once for all M rows.
+ * Source: spark_model gemm_quant.rs, dense_gemv_batchm (the contract: one weight sweep for M <= 8 rows,
+ * refusal of any other M); inferencelayer kernel_lab.rs, GEMV_F16S with KC columns per workgroup.
+ *   Y float[M][N] (row-major), X float[M][K] (row-major, 16-byte aligned); other arguments as q4_gemv.
+ *   1 <= M <= 8. Row m of Y equals q4_gemv on X[m] up to fp32 summation order.
+ */
+int q4_gemv_batched(float *Y, const uint8_t *qs, const uint16_t *d, const float *X, int M, int N, int K,
+                    q4_stream_t stream);
+
+/*
+ * y[n] = sum_k W[n][k] * xhat[k], xhat[k] = x[k] * r * gamma[k], r = 1 / sqrt(sum_k x[k]^2 / K + eps).
+ * The normalised input stays in shared memory; it is never written to global memory.
+ * Source: trueno-gpu fused.rs, FusedRmsNormQ4KGemvKernel (phases 1-3).
+ *   y float[N]; w uint8[N][K/256][144] Q4_K (16-byte aligned); x, gamma float[K] (16-byte aligned);
+ *   eps >= 0 and finite (1e-5 is the page's default). N >= 1; K >= 256 and K % 256 == 0.
+ */
+int fused_rmsnorm_q4k_gemv(float *y, const uint8_t *w, const float *x, const float *gamma, float eps, int N,
+                           int K, q4_stream_t stream);
+
+/*
+ * y_gate[n] = sum_k Wg[n][k] * xhat[k] and y_up[n] = sum_k Wu[n][k] * xhat[k] from one staged input.
+ * gamma != NULL: xhat is the RMSNorm of x as in fused_rmsnorm_q4k_gemv; gamma == NULL: xhat = x.
+ * Source: trueno-gpu fused.rs, FusedGateUpQ4KGemvKernel (with the full Q4_K decode for both projections).
+ *   y_gate, y_up float[N]; w_gate, w_up uint8[N][K/256][144] (16-byte aligned); x float[K] and gamma
+ *   float[K] or NULL (16-byte aligned). N >= 1; K >= 256 and K % 256 == 0; eps as above.
+ */
+int fused_gateup_q4k_gemv(float *y_gate, float *y_up, const uint8_t *w_gate, const uint8_t *w_up,
+                          const float *x, const float *gamma, float eps, int N, int K, q4_stream_t stream);
+
+/*
+ * Expert-gathered MoE gate and up GEMV over planar Q4 expert stores.
+ * For token t < T and slot s < topk with e = expert_ids[t*topk + s]:
+ *   y_gate[(t*topk + s)*N + r] = sum_k Wg[e*N + r][k] * x[t][k],  likewise y_up with Wu, for r < N.
+ * Each selected expert's rows are streamed once per call and applied to every token routed to it; the
+ * routing is read on the device (no host synchronisation).
+ * Source: inferencelayer kernel_lab.rs, moe_lab and the MoE ceiling shader (row = eid*MI + r, one output
+ * per routed row, gate and up stores).
+ *   qs_gate, qs_up uint8[E*N][K/32][16]; d_gate, d_up uint16[E*N][K/32]; x float[T][K] (16-byte aligned);
+ *   expert_ids int32[T][topk] (device). 1 <= topk <= E; T*topk <= 512.
+ *   A slot whose id is outside [0, E) gets NaN outputs and, when dev_status is not NULL, *dev_status is
+ *   set to Q4_FAULT_BAD_EXPERT (dev_status is a device int32 the caller zeroes beforehand).
+ */
+int moe_q4_gemv(float *y_gate, float *y_up, const uint8_t *qs_gate, const uint16_t *d_gate, const uint8_t *qs_up,
+                const uint16_t *d_up, const float *x, const int32_t *expert_ids, int T, int topk, int E, int N,
+                int K, int32_t *dev_status, q4_stream_t stream);
+
+/*
+ * Pure-read ceiling instruments: the same bytes, the same addressing and the same launch shape as the
+ * matching GEMV, but no unpack and no dot products. Each output row receives the XOR of the 32-bit quant
+ * words and zero-extended 16-bit scales (Q4) or of the 32-bit words of the super-blocks (Q4_K) of that
+ * row, stored as raw bits in a float, so nothing can be optimised away and the result is checkable.
+ * Source: inferencelayer kernel_lab.rs, the `pure_read` probe and MOE_PURE_READ ("pureread ~ kernel"
+ * means the access pattern is the limit; "pureread >> kernel" means the arithmetic is).
+ *   q4_pure_read:  sink float[N]; other arguments as q4_gemv.
+ *   q4k_pure_read: sink float[N]; w as fused_rmsnorm_q4k_gemv.
+ *   moe_q4_pure_read: sink_gate, sink_up float[T][topk][N]; other arguments as moe_q4_gemv; a slot with
+ *   an id outside [0, E) gets NaN.
+ */
+int q4_pure_read(float *sink, const uint8_t *qs, const uint16_t *d, int N, int K, q4_stream_t stream);
+int q4k_pure_read(float *sink, const uint8_t *w, int N, int K, q4_stream_t stream);
+int moe_q4_pure_read(float *sink_gate, float *sink_up, const uint8_t *qs_gate, const uint16_t *d_gate,
+                     const uint8_t *qs_up, const uint16_t *d_up, const int32_t *expert_ids, int T, int topk,
+                     int E, int N, int K, int32_t *dev_status, q4_stream_t stream);
+
+/*
+ * Dequant dumps (debug): W[n][k] = the fp32 weight, bit-exact with the format definitions above
+ * ((q - 8) * d for Q4; d*sc*q - dmin*m rounded once to fp32 for Q4_K).
+ *   W float[N][K] (16-byte aligned); other arguments as q4_gemv / fused_rmsnorm_q4k_gemv.
+ */
+int q4_dequant(float *W, const uint8_t *qs, const uint16_t *d, int N, int K, q4_stream_t stream);
+int q4k_dequant(float *W, const uint8_t *w, int N, int K, q4_stream_t stream);
+
+/* Text of the calling thread's most recent refusal or failure ("" when none). Valid until the next call. */
+const char *q4_last_error(void);
+
+/*
+ * Synchronises the current device, then ORs the fault bits every kernel family recorded since the last
+ * call into *faults and clears them. Returns Q4_OK or Q4_ECUDA.
+ */
+int q4_device_faults(unsigned *faults);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4GEMV_H */

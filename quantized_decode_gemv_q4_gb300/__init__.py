@@ -1,0 +1,219 @@
+"""GB300 4-bit decode GEMVs: a thin Python binding over the C ABI in ``include/q4gemv.h``.
+
+Each function has the name of its C entry point and takes CUDA tensors (PyTorch is used only for
+device memory and streams). Shapes give the sizes; the call is enqueued on the given stream (default:
+the current stream) and returns at once. A refusal or a CUDA failure raises :class:`Q4Error` with the
+library's message. There is no CPU path: without the compiled library every call raises.
+
+Layouts (row-major, little-endian):
+  * Q4 planar: ``qs`` uint8 ``[N, K/32, 16]`` (or ``[N, K/2]``), ``d`` float16 ``[N, K/32]``.
+  * Q4_K: ``w`` uint8 ``[N, K/256, 144]`` (or ``[N, K/256*144]``).
+  * inputs and outputs float32.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
+    "moe_q4_gemv", "q4_pure_read", "q4k_pure_read", "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
+    "q4_device_faults", "FAULT_BAD_EXPERT",
+]
+
+Q4_OK, Q4_EINVAL, Q4_EALIGN, Q4_ECUDA, Q4_EUNSUPPORTED = 0, -1, -2, -3, -4
+FAULT_BAD_EXPERT = 4
+_CODE_NAMES = {Q4_EINVAL: "EINVAL", Q4_EALIGN: "EALIGN", Q4_ECUDA: "ECUDA", Q4_EUNSUPPORTED: "EUNSUPPORTED"}
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_CODE_NAMES.get(code, code)}: {message}")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+_SIGNATURES = {
+    "q4_gemv": [_P, _P, _P, _P, _I, _I, _P],
+    "q4_gemv_batched": [_P, _P, _P, _P, _I, _I, _I, _P],
+    "fused_rmsnorm_q4k_gemv": [_P, _P, _P, _P, ctypes.c_float, _I, _I, _P],
+    "fused_gateup_q4k_gemv": [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _P],
+    "moe_q4_gemv": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
+    "q4_pure_read": [_P, _P, _P, _I, _I, _P],
+    "q4k_pure_read": [_P, _P, _I, _I, _P],
+    "moe_q4_pure_read": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
+    "q4_dequant": [_P, _P, _P, _I, _I, _P],
+    "q4k_dequant": [_P, _P, _I, _I, _P],
+    "q4_device_faults": [ctypes.POINTER(ctypes.c_uint)],
+}
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (once) the compiled library; raise if it was never built."""
+    global _lib
+    if _lib is None:
+        p = path or lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"libq4gemv is not built ({p} missing): run quantized_decode_gemv_q4_gb300/build.py")
+        L = ctypes.CDLL(p)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.q4_last_error.argtypes = []
+        L.q4_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != Q4_OK:
+        raise Q4Error(rc, load().q4_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype, name: str) -> int | None:
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _q4_dims(qs: torch.Tensor, d: torch.Tensor):
+    N = d.shape[0]
+    K = d.numel() // N * 32
+    if qs.numel() != N * K // 2:
+        raise ValueError(f"qs holds {qs.numel()} bytes, expected N*K/2 = {N * K // 2}")
+    return N, K
+
+
+def _q4k_dims(w: torch.Tensor):
+    N = w.shape[0]
+    if (w.numel() // N) % 144:
+        raise ValueError("Q4_K rows must be a whole number of 144-byte super-blocks")
+    return N, w.numel() // N // 144 * 256
+
+
+def q4_gemv(y, qs, d, x, stream=None) -> None:
+    N, K = _q4_dims(qs, d)
+    if x.numel() != K or y.numel() != N:
+        raise ValueError("x must hold K values and y N values")
+    _check(load().q4_gemv(_ptr(y, torch.float32, "y"), _ptr(qs, torch.uint8, "qs"), _ptr(d, torch.float16, "d"),
+                          _ptr(x, torch.float32, "x"), N, K, _stream(stream)))
+
+
+def q4_gemv_batched(Y, qs, d, X, stream=None) -> None:
+    N, K = _q4_dims(qs, d)
+    M = X.shape[0] if X.dim() == 2 else 1
+    if X.numel() != M * K or Y.numel() != M * N:
+        raise ValueError("X must be [M, K] and Y [M, N]")
+    _check(load().q4_gemv_batched(_ptr(Y, torch.float32, "Y"), _ptr(qs, torch.uint8, "qs"),
+                                  _ptr(d, torch.float16, "d"), _ptr(X, torch.float32, "X"), M, N, K,
+                                  _stream(stream)))
+
+
+def fused_rmsnorm_q4k_gemv(y, w, x, gamma, eps: float = 1e-5, stream=None) -> None:
+    N, K = _q4k_dims(w)
+    if x.numel() != K or gamma.numel() != K or y.numel() != N:
+        raise ValueError("x and gamma must hold K values and y N values")
+    _check(load().fused_rmsnorm_q4k_gemv(_ptr(y, torch.float32, "y"), _ptr(w, torch.uint8, "w"),
+                                         _ptr(x, torch.float32, "x"), _ptr(gamma, torch.float32, "gamma"),
+                                         float(eps), N, K, _stream(stream)))
+
+
+def fused_gateup_q4k_gemv(y_gate, y_up, w_gate, w_up, x, gamma=None, eps: float = 1e-5, stream=None) -> None:
+    N, K = _q4k_dims(w_gate)
+    if _q4k_dims(w_up) != (N, K) or x.numel() != K or y_gate.numel() != N or y_up.numel() != N:
+        raise ValueError("gate and up must be [N, K/256, 144], x K values, outputs N values")
+    if gamma is not None and gamma.numel() != K:
+        raise ValueError("gamma must hold K values")
+    _check(load().fused_gateup_q4k_gemv(_ptr(y_gate, torch.float32, "y_gate"), _ptr(y_up, torch.float32, "y_up"),
+                                        _ptr(w_gate, torch.uint8, "w_gate"), _ptr(w_up, torch.uint8, "w_up"),
+                                        _ptr(x, torch.float32, "x"), _ptr(gamma, torch.float32, "gamma"),
+                                        float(eps), N, K, _stream(stream)))
+
+
+def _moe_dims(qs_gate, d_gate, expert_ids, E):
+    rows, K = _q4_dims(qs_gate, d_gate)
+    if rows % E:
+        raise ValueError("the expert stores must hold E*N rows")
+    T, topk = expert_ids.shape
+    return T, topk, rows // E, K
+
+
+def moe_q4_gemv(y_gate, y_up, qs_gate, d_gate, qs_up, d_up, x, expert_ids, E: int, dev_status=None,
+                stream=None) -> None:
+    T, topk, N, K = _moe_dims(qs_gate, d_gate, expert_ids, E)
+    if x.numel() != T * K or y_gate.numel() != T * topk * N or y_up.numel() != T * topk * N:
+        raise ValueError("x must be [T, K] and outputs [T, topk, N]")
+    _check(load().moe_q4_gemv(_ptr(y_gate, torch.float32, "y_gate"), _ptr(y_up, torch.float32, "y_up"),
+                              _ptr(qs_gate, torch.uint8, "qs_gate"), _ptr(d_gate, torch.float16, "d_gate"),
+                              _ptr(qs_up, torch.uint8, "qs_up"), _ptr(d_up, torch.float16, "d_up"),
+                              _ptr(x, torch.float32, "x"), _ptr(expert_ids, torch.int32, "expert_ids"),
+                              T, topk, E, N, K, _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def q4_pure_read(sink, qs, d, stream=None) -> None:
+    N, K = _q4_dims(qs, d)
+    _check(load().q4_pure_read(_ptr(sink, torch.float32, "sink"), _ptr(qs, torch.uint8, "qs"),
+                               _ptr(d, torch.float16, "d"), N, K, _stream(stream)))
+
+
+def q4k_pure_read(sink, w, stream=None) -> None:
+    N, K = _q4k_dims(w)
+    _check(load().q4k_pure_read(_ptr(sink, torch.float32, "sink"), _ptr(w, torch.uint8, "w"), N, K,
+                                _stream(stream)))
+
+
+def moe_q4_pure_read(sink_gate, sink_up, qs_gate, d_gate, qs_up, d_up, expert_ids, E: int, dev_status=None,
+                     stream=None) -> None:
+    T, topk, N, K = _moe_dims(qs_gate, d_gate, expert_ids, E)
+    _check(load().moe_q4_pure_read(_ptr(sink_gate, torch.float32, "sink_gate"), _ptr(sink_up, torch.float32, "sink_up"),
+                                   _ptr(qs_gate, torch.uint8, "qs_gate"), _ptr(d_gate, torch.float16, "d_gate"),
+                                   _ptr(qs_up, torch.uint8, "qs_up"), _ptr(d_up, torch.float16, "d_up"),
+                                   _ptr(expert_ids, torch.int32, "expert_ids"), T, topk, E, N, K,
+                                   _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def q4_dequant(W, qs, d, stream=None) -> None:
+    N, K = _q4_dims(qs, d)
+    if W.numel() != N * K:
+        raise ValueError("W must be [N, K]")
+    _check(load().q4_dequant(_ptr(W, torch.float32, "W"), _ptr(qs, torch.uint8, "qs"), _ptr(d, torch.float16, "d"),
+                             N, K, _stream(stream)))
+
+
+def q4k_dequant(W, w, stream=None) -> None:
+    N, K = _q4k_dims(w)
+    if W.numel() != N * K:
+        raise ValueError("W must be [N, K]")
+    _check(load().q4k_dequant(_ptr(W, torch.float32, "W"), _ptr(w, torch.uint8, "w"), N, K, _stream(stream)))
+
+
+def q4_device_faults() -> int:
+    """Synchronise the device and return (and clear) the fault bits the kernels recorded."""
+    out = ctypes.c_uint(0)
+    _check(load().q4_device_faults(ctypes.byref(out)))
+    return out.value

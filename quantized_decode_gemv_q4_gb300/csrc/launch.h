@@ -1,0 +1,45 @@
+// Internal host-side interface between the C ABI (abi.cu) and the kernel translation units.
+// Arguments reaching these functions have already been validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4 {
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;  // bytes of dynamic shared memory a CTA may opt into
+    int major = 0, minor = 0;
+};
+
+// Cached per-device properties of the current device (thread-safe after first call).
+cudaError_t current_device_info(DeviceInfo* out);
+
+// ---- planar Q4 (32-weight blocks, f16 scale per block) -------------------------------------------
+// Y[v][n] = sum_k W[n][k] * X[v][k] for v < V; V in 1..8. Returns cudaErrorNotSupported when the
+// staged input does not fit in shared memory.
+cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V, int N, int K,
+                           cudaStream_t s);
+// Same bytes, same addressing, no math: sink[n] = XOR of row n's quant words and (zero-extended) scales.
+cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
+cudaError_t launch_q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
+
+// ---- Q4_K (144-byte super-blocks of 256 weights) ------------------------------------------------------
+// One or two weight streams against one input; gamma == nullptr skips RMSNorm.
+cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
+                            const float* gamma, float eps, int N, int K, cudaStream_t s);
+cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s);
+cudaError_t launch_q4k_dequant(float* W, const uint8_t* w, int N, int K, cudaStream_t s);
+
+// ---- MoE expert-gathered planar Q4 gate+up ---------------------------------------------------------
+cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gate, const uint16_t* d_gate,
+                               const uint8_t* qs_up, const uint16_t* d_up, const float* x, const int32_t* ids,
+                               int T, int topk, int E, int N, int K, int32_t* dev_status, bool pure_read,
+                               cudaStream_t s);
+
+// ---- device fault word (set by the MoE kernels on an expert id outside [0, E)) --------------------
+cudaError_t read_and_clear_fault_moe(unsigned* out);
+
+}  // namespace q4

@@ -1,0 +1,117 @@
+"""Planar Q4 GEMV (single and batched), its pure-read instrument and dequant dump on the GPU, through the
+C ABI, against the fp64 oracle on the same seeded inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import Guarded, assert_close, cu
+
+pytestmark = pytest.mark.gpu
+
+import quantized_decode_gemv_q4_gb300 as q4  # noqa: E402
+
+
+def run_q4(inp, M=None):
+    qs, d = cu(inp["qs"]), cu(inp["d"])
+    N = inp["d"].shape[0]
+    X = inp["x"]
+    if M is None:
+        y = Guarded(N)
+        q4.q4_gemv(y.t, qs, d, cu(X[0]))
+        return y.result()
+    Y = Guarded(M, N)
+    q4.q4_gemv_batched(Y.t, qs, d, cu(X[:M]))
+    return Y.result()
+
+
+@pytest.mark.parametrize("N,K", [
+    (256, 1024),   # the 256x1024 workload
+    (1, 32),       # one row, one block
+    (7, 96),       # scales not 16-byte groupable (K % 256 != 0): plain scale loads
+    (13, 288),
+    (1000, 4128),  # 129 blocks: a ragged lane iteration, N % 4 != 0
+    (333, 8192),   # several chunks per row
+    (4099, 2048),
+])
+def test_q4_gemv_matches_oracle(N, K, oracle_lib):
+    inp = synth.make_q4_gemv(seed=N + K, N=N, K=K)
+    ref, bound = oracle_lib.q4_gemv(inp["qs"], inp["d"], inp["x"][0])
+    assert_close(run_q4(inp), ref, bound, f"q4_gemv {N}x{K}")
+
+
+def test_q4_gemv_full_size_14336x4096(oracle_lib):
+    inp = synth.make_q4_gemv(seed=0, N=14336, K=4096, M=8)
+    ref, bound = oracle_lib.q4_gemv_batched(inp["qs"], inp["d"], inp["x"])
+    assert_close(run_q4(inp), ref[0], bound[0], "q4_gemv 14336x4096")
+    for M in (1, 2, 4, 8):
+        assert_close(run_q4(inp, M), ref[:M], bound[:M], f"q4_gemv_batched M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_q4_gemv_batched_every_M(M, oracle_lib):
+    inp = synth.make_q4_gemv(seed=100 + M, N=517, K=2048, M=M)
+    ref, bound = oracle_lib.q4_gemv_batched(inp["qs"], inp["d"], inp["x"])
+    assert_close(run_q4(inp, M), ref, bound, f"batched M={M}")
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_batched_rows_are_bit_identical_to_single_calls(M):
+    """Row t of the batched call equals the single-vector call on x_t, bit for bit: each row keeps its own
+    accumulator, summation order and cross-lane reduction tree whatever M is."""
+    inp = synth.make_q4_gemv(seed=7, N=14336, K=4096, M=M)
+    Y = run_q4(inp, M)
+    for t in range(M):
+        one = dict(inp, x=inp["x"][t:t + 1])
+        assert np.array_equal(run_q4(one).view(np.uint32), Y[t].view(np.uint32)), f"row {t}"
+
+
+def test_degenerate_blocks(oracle_lib):
+    rng = np.random.default_rng(5)
+    N, K = 64, 1024
+    d = rng.uniform(1e-3, 1e-2, (N, K // 32)).astype(np.float16)
+    x = rng.standard_normal((1, K)).astype(np.float32)
+    # every code 8: every weight is zero, so is every output
+    y = run_q4(dict(qs=np.full((N, K // 32, 16), 0x88, np.uint8), d=d, x=x))
+    assert np.all(y == 0.0)
+    # every code 0: -8 * sum_b d_b * S_b
+    inp = dict(qs=np.zeros((N, K // 32, 16), np.uint8), d=d, x=x)
+    ref, bound = oracle_lib.q4_gemv(inp["qs"], d, x[0])
+    assert_close(run_q4(inp), ref, bound, "all codes 0")
+    # large and tiny inputs keep relative accuracy (the staged input is pre-scaled by up to 2^23)
+    for scale in (1e20, 1e-30):
+        inp = dict(qs=rng.integers(0, 256, (N, K // 32, 16), dtype=np.uint8), d=d, x=(x * scale).astype(np.float32))
+        ref, bound = oracle_lib.q4_gemv(inp["qs"], d, inp["x"][0])
+        assert_close(run_q4(inp) / scale, ref / scale, bound / scale, f"x scaled by {scale}")
+
+
+def test_pure_read_touches_exactly_the_weight_bytes():
+    for N, K in ((256, 1024), (14336, 4096), (19, 96)):
+        qs, d = synth.q4_weights(np.random.default_rng(N), N, K)
+        sink = Guarded(N)
+        q4.q4_pure_read(sink.t, cu(qs), cu(d))
+        got = sink.result().view(np.uint32)
+        words = np.bitwise_xor.reduce(qs.reshape(N, -1).view("<u4"), axis=1)
+        scales = np.bitwise_xor.reduce(d.view(np.uint16).astype(np.uint32), axis=1)
+        assert np.array_equal(got, words ^ scales)
+
+
+@pytest.mark.parametrize("N,K", [(256, 1024), (37, 96), (3000, 4096)])
+def test_q4_dequant_is_bit_exact(N, K, oracle_lib):
+    qs, d = synth.q4_weights(np.random.default_rng(K), N, K)
+    W = Guarded(N, K)
+    q4.q4_dequant(W.t, cu(qs), cu(d))
+    assert np.array_equal(W.result().view(np.uint32), oracle_lib.dequant_q4(qs, d).view(np.uint32))
+
+
+def test_refusals_on_device():
+    qs, d = synth.q4_weights(np.random.default_rng(1), 8, 64)
+    X = torch.zeros(9, 64, device="cuda")
+    Y = torch.empty(9, 8, device="cuda")
+    with pytest.raises(q4.Q4Error, match="outside 1..8"):
+        q4.q4_gemv_batched(Y, cu(qs), cu(d), X)
+
+
+def test_no_fault_bits_after_the_suite():
+    assert q4.q4_device_faults() == 0

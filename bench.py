@@ -1,0 +1,548 @@
+"""Benchmark of the 4-bit decode GEMVs on GB300.
+
+One step is one call of every GEMV entry point on its workload:
+  q4_gemv 256x1024, fused_rmsnorm_q4k_gemv 3584x3584, fused_gateup_q4k_gemv 2x18944x3584,
+  q4_gemv_batched 14336x4096 at M = 1, 2, 4 and 8, and moe_q4_gemv (64 experts x 1408x2048, 8 tokens x top-8).
+The metric is effective weight bandwidth: the weight bytes each call must read (for MoE, the distinct selected
+experts' bytes) divided by device time. Steps replay CUDA graphs over two replica sets of all weights, so each
+call reads weights that were last touched about 650 MB of traffic earlier (the L2 holds 129 MB).
+
+Prints one JSON line (rank 0). ``--impl reference`` times the plain-C fp64 oracle instead (host cores).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 2**20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = ["device_common.cuh", "kernels_q4.cu", "kernels_q4k.cu", "kernels_moe.cu"]
+
+
+# ------------------------------------------------------------------------------------------------
+# workload definition (shared by both arms)
+# ------------------------------------------------------------------------------------------------
+
+def q4_bytes(N, K):
+    return N * K // 2 + N * (K // 32) * 2
+
+
+def q4k_bytes(N, K):
+    return N * (K // 256) * 144
+
+
+def make_inputs(seed=0):
+    c1 = synth.make_q4_gemv(seed, 256, 1024)
+    c2 = synth.make_fused_rmsnorm(seed + 1, 3584, 3584)
+    c3 = synth.make_gateup(seed + 2, 18944, 3584)
+    c4 = synth.make_q4_gemv(seed + 3, 14336, 4096, M=8)
+    c5 = synth.make_moe(seed + 4, 64, 1408, 2048, 8, 8)
+    return c1, c2, c3, c4, c5
+
+
+def call_table(c5_ids):
+    """(name, weight bytes, key) of each call of a step, in launch order."""
+    uniq = len(np.unique(c5_ids))
+    return [
+        ("q4_gemv 256x1024", q4_bytes(256, 1024), "q4_gemv_256x1024"),
+        ("fused_rmsnorm_q4k_gemv 3584x3584", q4k_bytes(3584, 3584), "rmsnorm_q4k_3584x3584"),
+        ("fused_gateup_q4k_gemv 2x18944x3584", 2 * q4k_bytes(18944, 3584), "gateup_q4k_2x18944x3584"),
+        ("q4_gemv_batched 14336x4096 M=1", q4_bytes(14336, 4096), "q4_batched_14336x4096_m1"),
+        ("q4_gemv_batched 14336x4096 M=2", q4_bytes(14336, 4096), "q4_batched_14336x4096_m2"),
+        ("q4_gemv_batched 14336x4096 M=4", q4_bytes(14336, 4096), "q4_batched_14336x4096_m4"),
+        ("q4_gemv_batched 14336x4096 M=8", q4_bytes(14336, 4096), "q4_batched_14336x4096_m8"),
+        (f"moe_q4_gemv e64 1408x2048 t8k8 ({uniq} experts)", 2 * uniq * q4_bytes(1408, 2048), "moe_q4_e64_t8k8"),
+    ]
+
+
+WORKLOAD_NAME = ("decode GEMV suite: Q4 256x1024; RMSNorm+Q4_K 3584x3584; gate+up Q4_K 2x18944x3584; "
+                 "Q4 14336x4096 at M=1,2,4,8; MoE Q4 64x(1408x2048) gate+up, 8 tokens top-8")
+
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_decode_gemv_q4_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, or None when absent or stale."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    cur = kernel_source_hash()
+    for parts in lines:
+        if len(parts) >= 3 and parts[0] == kernel_key and parts[2] == cur:
+            return float(parts[1])
+    return None
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            smax = max(float(r[2]) for r in rows)
+            power = [float(r[3]) for r in rows]
+        except ValueError:
+            return None
+        # samples under load: power well above the idle floor
+        floor = min(power)
+        load = [s for s, p in zip(sm, power) if p > floor + 0.25 * (max(power) - floor)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------------
+# multi-rank plumbing
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate(per_rank_seconds: float, bytes_per_step: float, steps: int, world: int):
+    """Whole-job throughput: every rank runs the same step (independent replicas), timing is the slowest rank."""
+    t = max_over_ranks(per_rank_seconds, world)
+    return world * bytes_per_step * steps / t / 1e9, t
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg
+# ------------------------------------------------------------------------------------------------
+
+def oracle_step(o, inputs, frac=1.0):
+    """The step's work on the host oracle, on the first `frac` of each matrix's rows. Returns weight bytes."""
+    c1, c2, c3, c4, c5 = inputs
+    done = 0
+
+    def rows(n):
+        return max(1, int(round(n * frac)))
+
+    n = rows(256)
+    o.q4_gemv(c1["qs"][:n], c1["d"][:n], c1["x"][0])
+    done += q4_bytes(n, 1024)
+    n = rows(3584)
+    o.fused_rmsnorm_q4k_gemv(c2["w"][:n], c2["x"], c2["gamma"], c2["eps"])
+    done += q4k_bytes(n, 3584)
+    n = rows(18944)
+    o.fused_gateup_q4k_gemv(c3["w_gate"][:n], c3["w_up"][:n], c3["x"], c3["gamma"], c3["eps"])
+    done += 2 * q4k_bytes(n, 3584)
+    n = rows(14336)
+    for M in (1, 2, 4, 8):
+        o.q4_gemv_batched(c4["qs"][:n], c4["d"][:n], c4["x"][:M])
+        done += q4_bytes(n, 4096)
+    n = rows(1408)
+    per_expert = lambda a: np.ascontiguousarray(a.reshape(64, 1408, *a.shape[1:])[:, :n].reshape(64 * n, *a.shape[1:]))  # noqa: E731
+    o.moe_q4_gemv(per_expert(c5["qs_gate"]), per_expert(c5["d_gate"]), per_expert(c5["qs_up"]),
+                  per_expert(c5["d_up"]), c5["x"], c5["ids"], 64)
+    done += 2 * len(np.unique(c5["ids"])) * q4_bytes(n, 2048)
+    return done
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    o = oracle.default()
+    inputs = make_inputs()
+    t0 = time.perf_counter()
+    oracle_step(o, inputs, 1.0 / 64)
+    t_full = (time.perf_counter() - t0) * 64
+    frac = min(1.0 / 16, max(1.0 / 4096, 90.0 / ((args.steps + args.warmup) * t_full)))
+    for _ in range(args.warmup):
+        oracle_step(o, inputs, frac)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += oracle_step(o, inputs, frac)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    sample = (f"each step: the suite on the first {frac:.5f} of every matrix's rows (MoE: of every expert's rows), "
+              "sized so that warm-up plus timed steps take about 90 s")
+    line = {
+        "impl": "reference", "metric": "effective weight GB/s over the decode GEMV suite", "value": value,
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": WORKLOAD_NAME, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU leg
+# ------------------------------------------------------------------------------------------------
+
+class Suite:
+    """Device copies of the suite's weights (several replica sets) and its per-step inputs/outputs."""
+
+    def __init__(self, inputs, replicas: int, dev):
+        import torch
+
+        cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        c1, c2, c3, c4, c5 = inputs
+        self.inputs = inputs
+        self.sets = []
+        for _ in range(replicas):
+            self.sets.append(dict(
+                c1=(cu(c1["qs"]), cu(c1["d"])), c2=cu(c2["w"]), c3=(cu(c3["w_gate"]), cu(c3["w_up"])),
+                c4=[(cu(c4["qs"]), cu(c4["d"])) for _ in range(4)],  # one copy per batch width: each call cold
+                c5=(cu(c5["qs_gate"]), cu(c5["d_gate"]), cu(c5["qs_up"]), cu(c5["d_up"]))))
+        # per-step activations (device) and outputs
+        self.x1 = cu(c1["x"][0])
+        self.x2, self.g2 = cu(c2["x"]), cu(c2["gamma"])
+        self.x3, self.g3 = cu(c3["x"]), cu(c3["gamma"])
+        self.X4 = cu(c4["x"])
+        self.x5, self.ids5 = cu(c5["x"]), cu(c5["ids"])
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.y1 = torch.empty(256, **f32)
+        self.y2 = torch.empty(3584, **f32)
+        self.y3g, self.y3u = torch.empty(18944, **f32), torch.empty(18944, **f32)
+        self.Y4 = [torch.empty(M, 14336, **f32) for M in (1, 2, 4, 8)]
+        self.y5g, self.y5u = torch.empty(8, 8, 1408, **f32), torch.empty(8, 8, 1408, **f32)
+
+    def calls(self, s):
+        """The step's calls on replica set s, as closures in launch order."""
+        import quantized_decode_gemv_q4_gb300 as q4
+
+        w = self.sets[s]
+        c2eps = float(self.inputs[1]["eps"])
+        c3eps = float(self.inputs[2]["eps"])
+        out = [
+            lambda: q4.q4_gemv(self.y1, w["c1"][0], w["c1"][1], self.x1),
+            lambda: q4.fused_rmsnorm_q4k_gemv(self.y2, w["c2"], self.x2, self.g2, c2eps),
+            lambda: q4.fused_gateup_q4k_gemv(self.y3g, self.y3u, w["c3"][0], w["c3"][1], self.x3, self.g3, c3eps),
+        ]
+        for i, M in enumerate((1, 2, 4, 8)):
+            out.append(lambda i=i, M=M: q4.q4_gemv_batched(self.Y4[i], w["c4"][i][0], w["c4"][i][1], self.X4[:M]))
+        out.append(lambda: q4.moe_q4_gemv(self.y5g, self.y5u, *w["c5"], self.x5, self.ids5, 64))
+        return out
+
+
+def capture(fns, stream):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fns:
+            fn()
+    return g
+
+
+def run_gpu(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    q4.load()
+    inputs = make_inputs()
+    table = call_table(inputs[4]["ids"])
+    step_bytes = sum(t[1] for t in table)
+    replicas = 2
+    suite = Suite(inputs, replicas, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm every call once eagerly (plans, attributes), then capture one graph per replica set
+    with torch.cuda.stream(stream):
+        for s in range(replicas):
+            for fn in suite.calls(s):
+                fn()
+    torch.cuda.synchronize()
+    graphs = [capture(suite.calls(s), stream) for s in range(replicas)]
+    n_calls = len(table)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % replicas].replay()
+    torch.cuda.synchronize()
+
+    # ---- headline: K steps, device-timed ----------------------------------------------------------
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            start.record()
+            for i in range(args.steps):
+                graphs[i % replicas].replay()
+            end.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    secs = start.elapsed_time(end) / 1e3
+    value, tmax = aggregate(secs, step_bytes, args.steps, world)
+    clocks = clk.summary()
+
+    # ---- per-call device time: each call type alone, back to back in one graph over the replica sets ---
+    reps = 8 * replicas
+    kt_us = np.zeros(n_calls)
+    for j in range(n_calls):
+        fns = [suite.calls(i % replicas)[j] for i in range(reps)]
+        g = capture(fns, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        best = float("inf")
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record()
+                g.replay()
+                b.record()
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / reps * 1e3)
+        kt_us[j] = best
+        del g
+    peak, peak_kind = measured_peaks()
+    per_call = []
+    for (name, b, _), us in zip(table, kt_us):
+        per_call.append({"call": name, "us": round(float(us), 3), "weight_GBps": round(b / us / 1e3, 1),
+                         "frac_of_hbm_peak": round(b / us / 1e3 / peak, 4)})
+    dom = int(np.argmax(kt_us))
+    traffic = committed_traffic(table[dom][2])
+    achieved = table[dom][1] / kt_us[dom] / 1e3
+    roofline = {"bound": "hbm", "kernel": table[dom][0], "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "algorithmic_bytes": table[dom][1], "us_per_launch": round(float(kt_us[dom]), 3)}
+
+    # ---- end to end through the Python API with host buffers ---------------------------------------
+    e2e = run_e2e(suite, inputs, stream, max(20, min(args.steps // 20, 400)), table)
+
+    # ---- CPU baseline (oracle, host cores) -----------------------------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inputs)
+
+    if rank == 0:
+        line = {
+            "metric": "effective weight GB/s over the decode GEMV suite (weight bytes read / device time)",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tmax / args.steps * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (4-bit weights, fp32 inputs and accumulation)",
+            "data": "synthetic (seeded generators; no trained weights)",
+            "config": {"workload": WORKLOAD_NAME, "weight_bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2: 2 replica sets of all weights (846 MB), each call reads "
+                             "weights last touched ~650 MB of traffic earlier", "graph": "one CUDA graph per step",
+                       "parallelism": f"replicas x{world}"},
+            "per_call": per_call, "roofline": roofline, "gpu_launches": args.steps * n_calls,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(suite, inputs, stream, steps, table):
+    """Each step: copy the step's activations (and expert ids) from pinned host memory, make the eight calls
+    through the Python binding, read every output back to pinned host memory, wait for it."""
+    import torch
+
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    c1, c2, c3, c4, c5 = inputs
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_in = [pin(c1["x"][0]), pin(c2["x"]), pin(c2["gamma"]), pin(c3["x"]), pin(c3["gamma"]), pin(c4["x"]),
+            pin(c5["x"]), pin(c5["ids"])]
+    d_in = [suite.x1, suite.x2, suite.g2, suite.x3, suite.g3, suite.X4, suite.x5, suite.ids5]
+    d_out = [suite.y1, suite.y2, suite.y3g, suite.y3u, *suite.Y4, suite.y5g, suite.y5u]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    step_bytes = sum(t[1] for t in table)
+
+    def step(i):
+        with torch.cuda.stream(stream):
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            for fn in suite.calls(i % len(suite.sets)):
+                fn()
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(5):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    assert q4.q4_device_faults() == 0
+    return {"value": round(step_bytes * steps / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
+            "path": "python binding, eager launches, pinned host copies, one host sync per step"}
+
+
+def cpu_baseline(inputs):
+    import oracle
+
+    o = oracle.default()
+    t0 = time.perf_counter()
+    oracle_step(o, inputs, 1.0 / 64)
+    frac = min(1.0, 10.0 / ((time.perf_counter() - t0) * 64))  # aim at about 10 s of host work
+    t0 = time.perf_counter()
+    done = oracle_step(o, inputs, frac)
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one pass of the suite over the first {frac:.3f} of every matrix's rows (MoE: of every "
+                      f"expert's rows); {dt:.1f} s single-threaded fp64"}
+
+
+CASES = ["c1", "c2", "c3", "c4m1", "c4m2", "c4m4", "c4m8", "c5", "pure_q4", "pure_q4k", "pure_moe"]
+
+
+def run_case(args):
+    """A few plain calls of one workload (for profilers): no graphs, no timing, one replica."""
+    import torch
+
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    torch.cuda.set_device(0)
+    inputs = make_inputs()
+    suite = Suite(inputs, 1, torch.device("cuda", 0))
+    fns = suite.calls(0)
+    w = suite.sets[0]
+    pick = {"c1": fns[0], "c2": fns[1], "c3": fns[2], "c4m1": fns[3], "c4m2": fns[4], "c4m4": fns[5],
+            "c4m8": fns[6], "c5": fns[7],
+            "pure_q4": lambda: q4.q4_pure_read(suite.Y4[3][0], w["c4"][0][0], w["c4"][0][1]),
+            "pure_q4k": lambda: q4.q4k_pure_read(suite.y3g, w["c3"][0]),
+            "pure_moe": lambda: q4.moe_q4_pure_read(suite.y5g, suite.y5u, *w["c5"], suite.ids5, 64)}[args.case]
+    for _ in range(args.iters):
+        pick()
+    torch.cuda.synchronize()
+    assert q4.q4_device_faults() == 0
+    print(f"case {args.case}: {args.iters} calls ok", flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES, help="run a few calls of one workload (for profilers) and exit")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    if args.case:
+        return run_case(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -147,6 +147,105 @@ __device__ __forceinline__ Word8 decode_word(uint32_t w) {
 }
 
 // ------------------------------------------------------------------------------------------------
+// Bias-free nibble decode (subnormal codes) and block-scaled staging
+// ------------------------------------------------------------------------------------------------
+//
+// Masking a code that sits at bit p of a word leaves the float whose bit pattern is q << p, i.e. the exact
+// value q * 2^(p-149) (p <= 16, so the pattern stays below 2^23: a subnormal, whose value is the pattern read
+// as an integer times 2^-149). So one AND per code gives a float proportional to the unsigned code,
+// with no bias to remove. The matching input element is staged as x * 2^(127-p-e), where e bounds the
+// exponent of its 32-element block (every |x| of the block < 2^e); then each fp32x2 FMA adds exactly
+// q * x * 2^(-22-e) up to one rounding, far from both overflow and the subnormal range. A block's sum
+// A = sum q x * 2^(-22-e) is turned back with t = A * 2^(22+e) - 8 * sum(x), which also applies the
+// format's -8 offset, and the row accumulates d * t.
+// float4 loads each thread issues back to back while staging the input, before it uses any of them.
+constexpr int kStageU = 8;
+// Whole 32-element blocks (eight float4 each) a thread loads back to back while staging a planar-Q4 input.
+constexpr int kStageB = 2;
+
+// Sum and largest magnitude of one 32-element block held by one thread as eight float4 (fixed tree).
+__device__ __forceinline__ void block_sum_max(const float4 (&v)[8], float& sum, float& mx) {
+    float s[8], m[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        s[q] = (v[q].x + v[q].y) + (v[q].z + v[q].w);
+        m[q] = fmaxf(fmaxf(fabsf(v[q].x), fabsf(v[q].y)), fmaxf(fabsf(v[q].z), fabsf(v[q].w)));
+    }
+    sum = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+    mx = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+struct Word8s {
+    float2 lo01, lo23, hi01, hi23;  // (lo jj0, lo jj1), (lo jj2, lo jj3), (hi jj0, hi jj1), (hi jj2, hi jj3)
+};
+
+__device__ __forceinline__ Word8s decode_word_sub(uint32_t w) {
+    const uint32_t s = w >> 12;
+    Word8s r;
+    r.lo01 = make_float2(__uint_as_float(w & 0x0000000Fu), __uint_as_float(w & 0x00000F00u));
+    r.lo23 = make_float2(__uint_as_float(w & 0x000F0000u), __uint_as_float(s & 0x0000F000u));
+    r.hi01 = make_float2(__uint_as_float(w & 0x000000F0u), __uint_as_float(w & 0x0000F000u));
+    r.hi23 = make_float2(__uint_as_float(s & 0x00000F00u), __uint_as_float(s & 0x000F0000u));
+    return r;
+}
+
+// 2^k for -126 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+
+// Exponent bound e of a block from its largest magnitude m: m < 2^e, clamped to [-100, 128]. Blocks whose
+// largest magnitude is below 2^-101 stage with e = -100 (their elements are still represented exactly);
+// a non-finite element gives e = 128 and propagates.
+__device__ __forceinline__ int block_exponent(float m) {
+    const int ef = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+    if (ef == 255) return 128;
+    return max(ef - 126, -100);
+}
+
+// x * 2^(127-p-e) for the code position p of (half, jj), in two exact power-of-two steps (the exponent can
+// reach 227).
+__device__ __forceinline__ float stage_scaled(float x, int hi, uint32_t jj, int e) {
+    constexpr uint32_t lo_tab = 0u | (8u << 5) | (16u << 10) | (12u << 15);
+    constexpr uint32_t hi_tab = 4u | (12u << 5) | (8u << 10) | (16u << 15);
+    const int p = (int)(((hi ? hi_tab : lo_tab) >> (5u * jj)) & 31u);
+    const int k = 127 - p - e;
+    const int k1 = k >> 1;
+    return (x * pow2i(k1)) * pow2i(k - k1);
+}
+
+// Block factor 2^(22+e); +inf once that passes the float range (blocks with an element of magnitude 2^105
+// or more are outside the supported range and yield a non-finite result).
+__device__ __forceinline__ float block_factor(int e) { return 22 + e <= 127 ? pow2i(22 + e) : INFINITY; }
+
+// Sum and largest magnitude of 32 consecutive elements held as one float4 by each of 8 aligned lanes; every
+// lane of the group gets both (fixed summation tree).
+__device__ __forceinline__ void block8_sum_max(const float4& v, float& sum, float& mx) {
+    sum = (v.x + v.y) + (v.z + v.w);
+    mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+}
+
+// Chunk-major staged input: float[ceil(U/32)][V][8 quads][32 unit lanes][4] for V vectors of U units. A
+// lane that always works on units u = 32c + lane finds every quad of every vector at one base register plus
+// compile-time offsets, and a warp's 32 lanes read 512 consecutive bytes.
+__host__ __device__ __forceinline__ uint32_t xs_chunk_offset(uint32_t v, uint32_t q, uint32_t u, uint32_t V) {
+    return (((u >> 5) * V + v) * 8u + q) * 512u + (u & 31u) * 16u;
+}
+__host__ __device__ __forceinline__ uint32_t xs_chunk_bytes(uint32_t V, uint32_t U) {
+    return ((U + 31u) / 32u) * V * 4096u;
+}
+// Per-block (2^(22+e), -8 * block sum) pairs in the same order: float2[ceil(U/32)][V][32].
+__host__ __device__ __forceinline__ uint32_t aux_offset(uint32_t v, uint32_t u, uint32_t V) {
+    return ((u >> 5) * V + v) * 256u + (u & 31u) * 8u;
+}
+__host__ __device__ __forceinline__ uint32_t aux_bytes(uint32_t V, uint32_t U) {
+    return ((U + 31u) / 32u) * V * 256u;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Staged-input layout
 // ------------------------------------------------------------------------------------------------
 //

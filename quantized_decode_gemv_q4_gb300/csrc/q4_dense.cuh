@@ -1,0 +1,434 @@
+// Planar Q4 decode GEMV kernel template (sm_103a): single vector, small batch (V <= 8 vectors sharing one
+// sweep over the weights) and the pure-read ceiling instrument. Included by the kernels_q4*.cu translation
+// units, which instantiate disjoint sets of batch widths so that they compile in parallel.
+//
+// Format (inferencelayer `kernel_lab.rs`, shader GEMV_F16S): row n of the weight matrix is K/32 blocks;
+// block b of row n has 16 packed bytes qs[n][b][0..15] and one f16 scale d[n][b]. Byte j holds weight j
+// in its low nibble and weight j+16 in its high nibble; the weight is (q - 8) * d.
+//
+// Kernel shape (one persistent CTA of W warps per SM):
+//  * the V input vectors are staged once per CTA in shared memory, block by block: each element is
+//    pre-scaled for the bit position of its code and its block's exponent bound, and beside each block sit
+//    its factor 2^(22+e) and -8 times its sum (device_common.cuh, bias-free decode). With XREG (V = 1) every
+//    lane then copies the quads of its own units into registers, so the main loop reads no staged input;
+//  * every warp owns a ring of D shared-memory slots filled by warp-cooperative cp.async copies; a slot holds
+//    R consecutive rows x CB = 32*UPL blocks (quants, then scales), so each weight byte is read from HBM once
+//    and all V vectors use it. Whole rows of exactly CB blocks travel as one contiguous copy;
+//  * lane l handles units l, l+32, ... of every row in the slot, in increasing order whatever CB is, so
+//    the per-row summation order depends only on K: batched rows equal single-vector calls bit for bit;
+//  * per 32-bit word: one shift and eight ANDs turn the codes into floats, and four packed fp32x2 FMAs per
+//    vector accumulate against the staged quads; per block: t = A * 2^(22+e) - 8 * sum(x), then d * t;
+//  * the per-stage control is incremental (no division in the loop) and full chunks run unguarded;
+//  * at the end of a row group the R*V totals are summed across the warp with a transposing shuffle
+//    reduction and stored.
+#pragma once
+
+#include <algorithm>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace q4 {
+namespace dense {
+
+struct Q4Params {
+    float* y;
+    const uint8_t* qs;
+    const uint16_t* d;
+    const float* x;
+    int N, K, nblk;
+    int S;      // chunks per row
+    int jobs;   // row groups of R rows
+    int dcopy;  // scales travel in the slot (else each unit reads its scale from global memory)
+    uint32_t xs_off, aux_off, slots_off;
+};
+
+__host__ __device__ constexpr uint32_t round_up_u(uint32_t a, uint32_t b) { return (a + b - 1) / b * b; }
+
+template <int R, int UPL>
+__host__ __device__ constexpr uint32_t slot_bytes() {
+    return round_up_u((uint32_t)(R * 32 * UPL * 16 + R * 32 * UPL * 2), 128u);
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+template <int V, int R, int W, int D, int UPL, bool XREG, bool PURE, int NCH>
+__global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
+    static_assert(NCH == 1 || NCH == 2, "one or two accumulation chains per row and vector");
+    static_assert(!XREG || V == 1, "register-resident input holds one vector");
+    constexpr int CB = 32 * UPL;
+    constexpr uint32_t QROW = CB * 16u;
+    constexpr uint32_t QBYTES = R * QROW;
+    constexpr uint32_t SLOT = slot_bytes<R, UPL>();
+    constexpr int kThreads = W * 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t xs = s_base + p.xs_off;
+    const uint32_t aux = s_base + p.aux_off;
+    const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
+
+    // Warps are numbered across CTAs first so that a small job count still spreads over all SMs.
+    const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
+    const int Wtot = (int)gridDim.x * W;
+    const uint64_t pol = policy_evict_first();
+
+    // Issue pointer: the next stage to copy (job, chunk) and its slot. One commit group per call, empty
+    // once this warp has no stage left, so the wait below always counts D - 1 groups ahead.
+    int ijob = gw, ic = 0, islot = 0;
+    auto issue = [&]() {
+        if (ijob < p.jobs) {
+            const int r0 = ijob * R;
+            const int rv = min(R, p.N - r0);
+            const int b0 = ic * CB;
+            const int nb = min(CB, p.nblk - b0);
+            const uint32_t slot = ring + (uint32_t)islot * SLOT;
+            if (nb == CB && p.S == 1) {
+                warp_copy_async(slot, p.qs + (size_t)r0 * QROW, (uint32_t)rv * QROW, lane, pol);
+                if (p.dcopy)
+                    warp_copy_async(slot + QBYTES, p.d + (size_t)r0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
+            } else {
+                for (int r = 0; r < rv; ++r) {
+                    const size_t rb = (size_t)(r0 + r) * p.nblk + b0;
+                    warp_copy_async(slot + (uint32_t)r * QROW, p.qs + rb * 16, (uint32_t)(nb * 16), lane, pol);
+                    if (p.dcopy)
+                        warp_copy_async(slot + QBYTES + (uint32_t)(r * CB * 2), p.d + rb, (uint32_t)(nb * 2), lane,
+                                        pol);
+                }
+            }
+            if (++ic == p.S) {
+                ic = 0;
+                ijob += Wtot;
+            }
+            islot = islot + 1 == D ? 0 : islot + 1;
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue();
+
+    if constexpr (!PURE) {
+        // Stage the V vectors (X is [V][K]): each thread takes whole 32-element blocks, issues the eight
+        // float4 loads of kStageB blocks before using any, sums each block and finds its largest magnitude
+        // in registers, and stores it pre-scaled with its own exponent bound. Consecutive threads hold
+        // consecutive blocks, so each quad store of a warp covers 512 consecutive bytes.
+        const int nb_all = V * p.nblk;
+        for (int base = threadIdx.x; base < nb_all; base += kThreads * kStageB) {
+            float4 xv[kStageB][8];
+#pragma unroll
+            for (int j = 0; j < kStageB; ++j) {
+                const int blk = base + j * kThreads;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    xv[j][q] = blk < nb_all ? __ldg(reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + q)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kStageB; ++j) {
+                const int blk = base + j * kThreads;
+                if (blk < nb_all) {
+                    const int v = blk / p.nblk;
+                    const uint32_t u = (uint32_t)(blk - v * p.nblk);
+                    float bsum, bmax;
+                    block_sum_max(xv[j], bsum, bmax);
+                    const int e = block_exponent(bmax);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        // float4 q8 of the block holds elements 4*q8 .. 4*q8+3: half q8/4, word q8%4
+                        const int hi = q8 >> 2;
+                        const uint32_t a = xs + xs_chunk_offset((uint32_t)v, (uint32_t)q8, u, (uint32_t)V);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "f"(stage_scaled(xv[j][q8].x, hi, 0, e)), "f"(stage_scaled(xv[j][q8].y, hi, 1, e)),
+                                     "f"(stage_scaled(xv[j][q8].z, hi, 2, e)), "f"(stage_scaled(xv[j][q8].w, hi, 3, e))
+                                     : "memory");
+                    }
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset((uint32_t)v, u, (uint32_t)V)),
+                                 "f"(block_factor(e)), "f"(-8.0f * bsum)
+                                 : "memory");
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // Register-resident input (V = 1, whole rows in one chunk): the quads and block pairs of this lane's
+    // units. Quads of units past the row end are never used.
+    float4 xr[XREG ? UPL : 1][8];
+    float2 ar[XREG ? UPL : 1];
+    if constexpr (XREG) {
+#pragma unroll
+        for (int it = 0; it < UPL; ++it) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xr[it][q] = lds128f(xs + (uint32_t)(it * 4096 + q * 512) + (uint32_t)lane * 16u);
+            ar[it] = lds64f(aux + (uint32_t)(it * 256) + (uint32_t)lane * 8u);
+        }
+    }
+
+    float tot[R][V];
+    uint32_t fold[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        fold[r] = 0u;
+#pragma unroll
+        for (int v = 0; v < V; ++v) tot[r][v] = 0.f;
+    }
+
+    const int my_jobs = gw < p.jobs ? (p.jobs - 1 - gw) / Wtot + 1 : 0;
+    const int total = my_jobs * p.S;
+    int job = gw, c = 0, cslot = 0;
+    for (int g = 0; g < total; ++g) {
+        issue();                 // stage g + D - 1 into the slot consumed at g - 1
+        cp_async_wait<D - 1>();  // stage g has landed
+        __syncwarp();
+        const uint32_t slot = ring + (uint32_t)cslot * SLOT;
+        const int r0 = job * R;
+        const int rv = min(R, p.N - r0);
+        const int b0 = c * CB;
+        const int nb = min(CB, p.nblk - b0);
+        const uint32_t qb = slot + (uint32_t)lane * 16u;
+        const uint32_t db = slot + QBYTES + (uint32_t)lane * 2u;
+        const uint32_t xb = xs + (uint32_t)(b0 >> 5) * (uint32_t)(V * 4096) + (uint32_t)lane * 16u;
+        const uint32_t ab = aux + (uint32_t)(b0 >> 5) * (uint32_t)(V * 256) + (uint32_t)lane * 8u;
+
+        auto unit = [&](const int it) {
+            uint4 w[R];
+            float dsc[R];
+            uint32_t dbits[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                w[r] = lds128(qb + (uint32_t)r * QROW + (uint32_t)(it * 512));
+                if (p.dcopy)
+                    dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
+                else
+                    dbits[r] = r < rv ? (uint32_t)__ldg(p.d + (size_t)(r0 + r) * p.nblk + b0 + it * 32 + lane) : 0u;
+                dsc[r] = f16_bits_to_f32(dbits[r]);
+            }
+            if constexpr (PURE) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
+            } else {
+                // NCH = 1: one fp32x2 chain per row and vector; NCH = 2: low and high codes in separate chains
+                // (shorter dependency chains), added at the end of the unit.
+                float2 acc[R][V][NCH];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    Word8s d8[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        float4 xl, xh;
+                        if constexpr (XREG) {
+                            xl = xr[it][i];
+                            xh = xr[it][4 + i];
+                        } else {
+                            const uint32_t xa = xb + (uint32_t)((it * V + v) * 4096 + i * 512);
+                            xl = lds128f(xa);
+                            xh = lds128f(xa + 2048u);
+                        }
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][v][0];
+                            a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
+                            a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
+                            float2 b = NCH == 1 ? a : (i == 0 ? make_float2(0.f, 0.f) : acc[r][v][NCH - 1]);
+                            b = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), b);
+                            b = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), b);
+                            if constexpr (NCH == 2) acc[r][v][0] = a;
+                            acc[r][v][NCH - 1] = b;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    float2 fa;
+                    if constexpr (XREG)
+                        fa = ar[it];
+                    else
+                        fa = lds64f(ab + (uint32_t)((it * V + v) * 256));
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float2 sa = NCH == 1 ? acc[r][v][0] : fadd2(acc[r][v][0], acc[r][v][NCH - 1]);
+                        const float t = fmaf(sa.x + sa.y, fa.x, fa.y);
+                        tot[r][v] = fmaf(dsc[r], t, tot[r][v]);
+                    }
+                }
+            }
+        };
+        if constexpr (XREG || R * V <= 2) {
+            // short bodies: unrolled, so neighbouring units overlap; full chunks run unguarded
+            if (nb == CB) {
+#pragma unroll
+                for (int it = 0; it < UPL; ++it) unit(it);
+            } else {
+#pragma unroll
+                for (int it = 0; it < UPL; ++it)
+                    if (it * 32 + lane < nb) unit(it);
+            }
+        } else {
+            // long bodies (R*V independent chains already): one copy of the unit, so the loop stays in the
+            // instruction cache
+#pragma unroll 1
+            for (int it = 0; it < UPL; ++it)
+                if (it * 32 + lane < nb) unit(it);
+        }
+        __syncwarp();  // every lane is done with this slot before a later stage overwrites it
+
+        if (c == p.S - 1) {
+            if constexpr (PURE) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) fold[r] ^= __shfl_xor_sync(0xffffffffu, fold[r], off);
+                    if (lane == 0 && r < rv) p.y[r0 + r] = __uint_as_float(fold[r]);
+                    fold[r] = 0u;
+                }
+            } else {
+                constexpr int NV = R * V;
+                constexpr int P2 = NextPow2<NV>::value;
+                constexpr int L2 = log2_const<P2>();
+                float vals[P2];
+#pragma unroll
+                for (int i = 0; i < P2; ++i) vals[i] = 0.f;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        vals[r * V + v] = tot[r][v];
+                        tot[r][v] = 0.f;
+                    }
+                warp_transpose_reduce<P2>(vals, lane);
+                const int idx = lane >> (5 - L2);
+                const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
+                if (leader && idx < NV) {
+                    const int r = idx / V;
+                    const int v = idx - r * V;
+                    if (r < rv) p.y[(size_t)v * p.N + r0 + r] = vals[0];
+                }
+            }
+        }
+        if (++c == p.S) {
+            c = 0;
+            job += Wtot;
+        }
+        cslot = cslot + 1 == D ? 0 : cslot + 1;
+    }
+}
+
+// Developer override of the ring depth, read once from Q4GEMV_Q4_DEPTH. Used for tuning sweeps; the
+// defaults in the launchers come from such sweeps.
+inline int depth_override(int d) {
+    static int o = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* e = getenv("Q4GEMV_Q4_DEPTH");
+        if (e) o = atoi(e);
+    });
+    return o > 0 ? o : d;
+}
+
+template <int V, int R, int W, int D, int UPL, bool XREG, bool PURE, int NCH>
+cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N,
+                         int K, bool dcopy, cudaStream_t s) {
+    constexpr int CB = 32 * UPL;
+    const uint32_t nblk = (uint32_t)K / 32u;
+    const uint32_t xsb = PURE ? 0u : xs_chunk_bytes((uint32_t)V, nblk);
+    const uint32_t axb = PURE ? 0u : aux_bytes((uint32_t)V, nblk);
+    const uint32_t smem = xsb + axb + (uint32_t)(W * D) * slot_bytes<R, UPL>();
+    if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
+    if (XREG && (int)nblk > CB) return cudaErrorNotSupported;
+    auto kern = q4_gemv_kernel<V, R, W, D, UPL, XREG, PURE, NCH>;
+    static std::once_flag attr_once[64];
+    cudaError_t err = cudaSuccess;
+    std::call_once(attr_once[di.device & 63], [&] {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+    });
+    if (err != cudaSuccess) return err;
+    Q4Params p;
+    p.y = y;
+    p.qs = qs;
+    p.d = d;
+    p.x = x;
+    p.N = N;
+    p.K = K;
+    p.nblk = (int)nblk;
+    p.S = (int)((nblk + CB - 1) / CB);
+    p.jobs = (N + R - 1) / R;
+    p.dcopy = dcopy ? 1 : 0;
+    p.xs_off = 0;
+    p.aux_off = xsb;
+    p.slots_off = xsb + axb;
+    const int grid = std::min(di.sm_count, p.jobs);
+    kern<<<grid, W * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// The deepest ring among the instantiated depths {2, 3, 4, 5, 6, 8} not above DMAX nor `want` that fits.
+template <int V, int R, int W, int DMAX, int UPL, bool XREG, bool PURE, int NCH>
+cudaError_t launch_upl(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N,
+                       int K, bool dcopy, int want, cudaStream_t s) {
+    cudaError_t e = cudaErrorNotSupported;
+#define Q4_TRY_DEPTH(DD)                                                                              \
+    if constexpr (DMAX >= DD)                                                                         \
+        if (e == cudaErrorNotSupported && want >= DD)                                                 \
+            e = launch_fixed<V, R, W, DD, UPL, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, s);
+    Q4_TRY_DEPTH(8)
+    Q4_TRY_DEPTH(6)
+    Q4_TRY_DEPTH(5)
+    Q4_TRY_DEPTH(4)
+    Q4_TRY_DEPTH(3)
+#undef Q4_TRY_DEPTH
+    if (e == cudaErrorNotSupported) e = launch_fixed<V, R, W, 2, UPL, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, s);
+    return e;
+}
+
+// Units per lane: the whole row in one chunk up to min(K/32, 32*upl_max) blocks (UPL = 1, 2, 4), longer rows
+// in chunks of that size. With the input in shared memory, smaller chunks when the rings would not fit beside
+// it; register-resident input needs the whole row in one chunk.
+template <int V, int R, int W, int DMAX, bool XREG, bool PURE, int NCH = 1>
+cudaError_t launch(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N, int K,
+                   int depth, int upl_max, cudaStream_t s) {
+    const int nblk = K / 32;
+    const bool dcopy = (nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(d) & 15u) == 0);
+    depth = std::min(depth_override(depth), DMAX);
+    const int upl0 = std::min(nblk <= 32 ? 1 : nblk <= 64 ? 2 : 4, upl_max);
+    cudaError_t e = cudaErrorNotSupported;
+    if (upl0 == 4) e = launch_upl<V, R, W, DMAX, 4, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    if (e == cudaErrorNotSupported && (upl0 == 2 || (!XREG && upl0 > 2)))
+        e = launch_upl<V, R, W, DMAX, 2, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    if (e == cudaErrorNotSupported && (upl0 == 1 || !XREG))
+        e = launch_upl<V, R, W, DMAX, 1, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    return e;
+}
+
+// Developer override of the batched variant (rows per lane and warps), read once from Q4GEMV_Q4_VB
+// (48: 4 rows x 8 warps; 216: 2 rows x 16 warps; 28: 2 rows x 8 warps). Used for tuning sweeps.
+inline int batched_variant() {
+    static int o = 48;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* e = getenv("Q4GEMV_Q4_VB");
+        if (e) o = atoi(e);
+    });
+    return o;
+}
+
+// Per-translation-unit entry points (kernels_q4_*.cu).
+cudaError_t gemv_v1(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int N, int K,
+                    cudaStream_t s);
+cudaError_t gemv_v2_4(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
+                      int N, int K, cudaStream_t s);
+cudaError_t gemv_v5_8(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
+                      int N, int K, cudaStream_t s);
+
+}  // namespace dense
+}  // namespace q4

@@ -72,9 +72,12 @@ def test_degenerate_blocks(oracle_lib):
     N, K = 64, 1024
     d = rng.uniform(1e-3, 1e-2, (N, K // 32)).astype(np.float16)
     x = rng.standard_normal((1, K)).astype(np.float32)
-    # every code 8: every weight is zero, so is every output
-    y = run_q4(dict(qs=np.full((N, K // 32, 16), 0x88, np.uint8), d=d, x=x))
-    assert np.all(y == 0.0)
+    # every code 8: every weight is zero, so the reference is exactly zero with a zero bound; the kernel sums
+    # q * x and subtracts 8 * sum(x) per block, so it must land within the absolute part of the tolerance
+    inp = dict(qs=np.full((N, K // 32, 16), 0x88, np.uint8), d=d, x=x)
+    ref, bound = oracle_lib.q4_gemv(inp["qs"], d, x[0])
+    assert np.all(ref == 0.0) and np.all(bound == 0.0)
+    assert_close(run_q4(inp), ref, bound, "all codes 8")
     # every code 0: -8 * sum_b d_b * S_b
     inp = dict(qs=np.zeros((N, K // 32, 16), np.uint8), d=d, x=x)
     ref, bound = oracle_lib.q4_gemv(inp["qs"], d, x[0])
@@ -84,6 +87,15 @@ def test_degenerate_blocks(oracle_lib):
         inp = dict(qs=rng.integers(0, 256, (N, K // 32, 16), dtype=np.uint8), d=d, x=(x * scale).astype(np.float32))
         ref, bound = oracle_lib.q4_gemv(inp["qs"], d, inp["x"][0])
         assert_close(run_q4(inp) / scale, ref / scale, bound / scale, f"x scaled by {scale}")
+    # blocks of very different magnitude in one vector, and all-zero blocks: each block is staged with its
+    # own exponent bound
+    xm = x.copy().reshape(K // 32, 32)
+    xm[0::4] *= 1e25
+    xm[1::4] *= 1e-25
+    xm[2::8] = 0.0
+    inp = dict(qs=rng.integers(0, 256, (N, K // 32, 16), dtype=np.uint8), d=d, x=xm.reshape(1, K))
+    ref, bound = oracle_lib.q4_gemv(inp["qs"], d, inp["x"][0])
+    assert_close(run_q4(inp), ref, bound, "mixed block magnitudes")
 
 
 def test_pure_read_touches_exactly_the_weight_bytes():

@@ -5,20 +5,28 @@
 // E*N rows per projection; slot (t, s) of token t uses expert e = ids[t*topk+s] and writes rows
 // (t*topk+s)*N + r of the gate and up outputs.
 //
-// Kernel shape (one persistent CTA of 8 warps per SM):
+// Kernel shape (one persistent CTA of W warps per SM):
 //  * prologue (every CTA, no host synchronisation): read the T*topk ids, find for each slot the first slot
 //    with the same expert and its rank among the slots of that expert, number the distinct experts in
-//    order of first appearance, and cut each expert's slot list into groups of at most MAXC slots; slots
+//    order of first appearance, and cut each expert's slot list into groups of at most kMaxC slots; slots
 //    with an id outside [0, E) get NaN outputs (written by CTA 0) and raise a status bit;
-//  * jobs are (group, row group of R rows); a warp streams the R gate rows and R up rows of its job through
-//    its own ring of cp.async slots, so each selected expert's bytes are read once per call (once per group
-//    when more than MAXC slots route to one expert) and every routed token reuses them;
-//  * all T input vectors are staged once per CTA (permuted, pre-scaled), and each decoded weight pair feeds
-//    one packed FMA per routed slot.
+//  * jobs are (group, projection, row group of R rows), numbered group-major; each warp owns one contiguous
+//    range of jobs, so it streams whole-row stages of consecutive rows through its own ring of cp.async
+//    slots with incremental control, and each selected expert's bytes are read once per call (once per
+//    group when more than kMaxC slots route to one expert);
+//  * all T input vectors are staged once per CTA, block by block, with the bias-free decode's per-block
+//    scaling (device_common.cuh): float[T][8 quads][K/32 units][4] and (2^(22+e), -8 * sum) pairs
+//    float2[T][K/32];
+//  * a job's slot count C (1..kMaxC) selects a compiled variant of the stage body, so each decoded code
+//    pair feeds exactly C packed FMAs; per block t = A * 2^(22+e) - 8 * sum(x), and the row accumulates
+//    d * t per routed slot;
+//  * at the end of a row group the R*C totals are summed across the warp with a transposing shuffle
+//    reduction and stored to each slot's output rows.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -43,8 +51,8 @@ struct MoEParams {
     const int32_t* ids;
     int32_t* status;
     int T, topk, E, N, K, nblk;
-    int CB, S, slot_bytes, d_off, dcopy;
-    uint32_t route_off, xs_off, slots_off;
+    int S, dcopy;
+    uint32_t route_off, xs_off, aux_off, slots_off;
     unsigned* fault;
 };
 
@@ -53,14 +61,27 @@ struct MoEParams {
 // group_cnt[kMaxSlots], scalars[4] (number of distinct experts, number of groups).
 constexpr int kRouteInts = 9 * kMaxSlots + 8;
 
-template <int R, int W, int D, bool PURE>
+__host__ __device__ constexpr uint32_t moe_slot_bytes(int R, int UPL) {
+    return (uint32_t)(((R * 32 * UPL * 18) + 127) / 128 * 128);
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+template <int R, int W, int D, int UPL, bool PURE>
 __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     constexpr int kThreads = W * 32;
+    constexpr int CB = 32 * UPL;
+    constexpr uint32_t QROW = CB * 16u;
+    constexpr uint32_t QBYTES = R * QROW;
+    constexpr uint32_t SLOT = moe_slot_bytes(R, UPL);
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int TK = p.T * p.topk;
-    const uint32_t U = (uint32_t)p.nblk;
 
     int* route = reinterpret_cast<int*>(smem + p.route_off);
     int* slot_ids = route;
@@ -178,237 +199,280 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     }
     __syncthreads();
 
-    // ---- weight streaming -----------------------------------------------------------------------------
+    // ---- jobs -------------------------------------------------------------------------------------------
     const uint32_t s_base = smem_addr(smem);
     const uint32_t xs = s_base + p.xs_off;
-    const uint32_t slots = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
+    const uint32_t aux = s_base + p.aux_off;
+    const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
+    const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
-    const int jobs = ngroups * rgs;
+    const int jobs = ngroups * 2 * rgs;
     const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
     const int Wtot = (int)gridDim.x * W;
-    const int my_jobs = gw < jobs ? (jobs - 1 - gw) / Wtot + 1 : 0;
-    const int total = my_jobs * p.S;
+    // this warp's contiguous range of jobs [j0, j1)
+    const int j0 = (int)(((long long)jobs * gw) / Wtot);
+    const int j1 = (int)(((long long)jobs * (gw + 1)) / Wtot);
     const uint64_t pol = policy_evict_first();
 
-    // Stage g of this warp -> slot g % D; one commit group per stage (empty when g >= total).
-    auto issue = [&](int g) {
-        if (g < total) {
-            const int job = gw + (g / p.S) * Wtot;
-            const int grp = job / rgs;
-            const int r0 = (job - grp * rgs) * R;
-            const int e = group_cnt[grp] >> 8;
-            const int c = g % p.S;
-            const int rv = min(R, p.N - r0);
-            const int b0 = c * p.CB;
-            const int nb = min(p.CB, p.nblk - b0);
-            const uint32_t slot = slots + (uint32_t)((g % D) * p.slot_bytes);
-            const size_t row0 = (size_t)e * p.N + r0;
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const uint8_t* q = s == 0 ? p.qg : p.qu;
-                const uint16_t* d = s == 0 ? p.dg : p.du;
-                const uint32_t qdst = slot + (uint32_t)(s * R * nb * 16);
-                const uint32_t ddst = slot + (uint32_t)(p.d_off + s * R * nb * 2);
-                if (p.S == 1) {
-                    warp_copy_async(qdst, q + row0 * p.nblk * 16, (uint32_t)(rv * nb * 16), lane, pol);
-                    if (p.dcopy) warp_copy_async(ddst, d + row0 * p.nblk, (uint32_t)(rv * nb * 2), lane, pol);
-                } else {
-                    for (int r = 0; r < rv; ++r) {
-                        const size_t rb = (row0 + r) * p.nblk + b0;
-                        warp_copy_async(qdst + (uint32_t)(r * nb * 16), q + rb * 16, (uint32_t)(nb * 16), lane, pol);
-                        if (p.dcopy)
-                            warp_copy_async(ddst + (uint32_t)(r * nb * 2), d + rb, (uint32_t)(nb * 2), lane, pol);
-                    }
+    // Job cursor: group, projection, row group, chunk. Jobs run group-major, then projection, then row
+    // group, so a warp's stages walk consecutive rows of one expert matrix.
+    struct Cursor {
+        int grp, sp, rg, c;
+    };
+    auto cursor_at = [&](int j) {
+        Cursor k;
+        k.grp = j / (2 * rgs);
+        const int rem = j - k.grp * 2 * rgs;
+        k.sp = rem / rgs;
+        k.rg = rem - k.sp * rgs;
+        k.c = 0;
+        return k;
+    };
+    auto advance = [&](Cursor& k) {
+        if (++k.c == p.S) {
+            k.c = 0;
+            if (++k.rg == rgs) {
+                k.rg = 0;
+                if (++k.sp == 2) {
+                    k.sp = 0;
+                    ++k.grp;
                 }
             }
+        }
+    };
+
+    const int total = (j1 - j0) * p.S;
+    Cursor ik = cursor_at(j0);
+    int issued = 0, islot = 0;
+    auto issue = [&]() {
+        if (issued < total) {
+            const int e = group_cnt[ik.grp] >> 8;
+            const int r0 = ik.rg * R;
+            const int rv = min(R, p.N - r0);
+            const int b0 = ik.c * CB;
+            const int nb = min(CB, p.nblk - b0);
+            const uint8_t* q = ik.sp == 0 ? p.qg : p.qu;
+            const uint16_t* d = ik.sp == 0 ? p.dg : p.du;
+            const size_t row0 = (size_t)e * p.N + r0;
+            const uint32_t slot = ring + (uint32_t)islot * SLOT;
+            if (nb == CB && p.S == 1) {
+                warp_copy_async(slot, q + row0 * QROW, (uint32_t)rv * QROW, lane, pol);
+                if (p.dcopy) warp_copy_async(slot + QBYTES, d + row0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
+            } else {
+                for (int r = 0; r < rv; ++r) {
+                    const size_t rb = (row0 + r) * p.nblk + b0;
+                    warp_copy_async(slot + (uint32_t)r * QROW, q + rb * 16, (uint32_t)(nb * 16), lane, pol);
+                    if (p.dcopy)
+                        warp_copy_async(slot + QBYTES + (uint32_t)(r * CB * 2), d + rb, (uint32_t)(nb * 2), lane, pol);
+                }
+            }
+            advance(ik);
+            ++issued;
+            islot = islot + 1 == D ? 0 : islot + 1;
         }
         cp_async_commit();
     };
 
-    for (int g = 0; g < D - 1; ++g) issue(g);
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue();
 
     if constexpr (!PURE) {
-        const int K4 = p.K >> 2;
-        for (int idx = threadIdx.x; idx < p.T * K4; idx += kThreads) {
-            const int v = idx / K4;
-            const uint32_t k = (uint32_t)(idx - v * K4) * 4u;
-            const float4 xv = __ldg(reinterpret_cast<const float4*>(p.x + (size_t)v * p.K + k));
-            uint32_t u, q, jj;
-            int hi;
-            q4_elem_place(k, u, q, jj, hi);
-            const uint32_t a = xs + xs_index((uint32_t)v, q, u, U) * 4u;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(xv.x * pos_scale_dev(hi, 0)),
-                         "f"(xv.y * pos_scale_dev(hi, 1)), "f"(xv.z * pos_scale_dev(hi, 2)),
-                         "f"(xv.w * pos_scale_dev(hi, 3))
-                         : "memory");
+        // Stage the T tokens block by block (each thread whole 32-element blocks, loads issued ahead).
+        const int nb_all = p.T * U;
+        for (int base = threadIdx.x; base < nb_all; base += kThreads * kStageB) {
+            float4 xv[kStageB][8];
+#pragma unroll
+            for (int j = 0; j < kStageB; ++j) {
+                const int blk = base + j * kThreads;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    xv[j][q] = blk < nb_all ? __ldg(reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + q)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kStageB; ++j) {
+                const int blk = base + j * kThreads;
+                if (blk < nb_all) {
+                    const int v = blk / U;
+                    const int u = blk - v * U;
+                    float bsum, bmax;
+                    block_sum_max(xv[j], bsum, bmax);
+                    const int e = block_exponent(bmax);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const int hi = q8 >> 2;
+                        const uint32_t a = xs + (uint32_t)(((v * 8 + q8) * U + u) * 16);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "f"(stage_scaled(xv[j][q8].x, hi, 0, e)), "f"(stage_scaled(xv[j][q8].y, hi, 1, e)),
+                                     "f"(stage_scaled(xv[j][q8].z, hi, 2, e)), "f"(stage_scaled(xv[j][q8].w, hi, 3, e))
+                                     : "memory");
+                    }
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((v * U + u) * 8)),
+                                 "f"(block_factor(e)), "f"(-8.0f * bsum)
+                                 : "memory");
+                }
+            }
         }
     }
     __syncthreads();
 
-    float2 tot[2][R][kMaxC];
-    uint32_t fold[2][R];
+    const uint32_t qstride = (uint32_t)U * 16u;  // bytes between the quads of one unit
+    float tot[R][kMaxC];
+    uint32_t fold[R];
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
+    for (int r = 0; r < R; ++r) {
+        fold[r] = 0u;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            fold[s][r] = 0u;
-#pragma unroll
-            for (int m = 0; m < kMaxC; ++m) tot[s][r][m] = make_float2(0.f, 0.f);
-        }
+        for (int m = 0; m < kMaxC; ++m) tot[r][m] = 0.f;
+    }
 
+    Cursor k = cursor_at(j0);
+    int cslot = 0;
     for (int g = 0; g < total; ++g) {
-        issue(g + D - 1);
-        cp_async_wait<D - 1>();
+        issue();                 // stage g + D - 1 into the slot consumed at g - 1
+        cp_async_wait<D - 1>();  // stage g has landed
         __syncwarp();
-        const uint32_t slot = slots + (uint32_t)((g % D) * p.slot_bytes);
-
-        const int job = gw + (g / p.S) * Wtot;
-        const int grp = job / rgs;
-        const int r0 = (job - grp * rgs) * R;
-        const int gc = group_cnt[grp];
+        const uint32_t slot = ring + (uint32_t)cslot * SLOT;
+        const int gc = group_cnt[k.grp];
         const int cnt = gc & 0xFF;
         const int e = gc >> 8;
-        const int first = group_first[grp];
-        const int c = g % p.S;
+        const int first = group_first[k.grp];
+        const int r0 = k.rg * R;
         const int rv = min(R, p.N - r0);
-        const int b0 = c * p.CB;
-        const int nb = min(p.CB, p.nblk - b0);
-        int tok[kMaxC];
-#pragma unroll
-        for (int m = 0; m < kMaxC; ++m) tok[m] = m < cnt ? list[first + m] / p.topk : 0;
+        const int b0 = k.c * CB;
+        const int nb = min(CB, p.nblk - b0);
+        const uint16_t* dglob = k.sp == 0 ? p.dg : p.du;
+        const uint32_t qb = slot + (uint32_t)lane * 16u;
+        const uint32_t db = slot + QBYTES + (uint32_t)lane * 2u;
 
-        for (int ul = lane; ul < nb; ul += 32) {
-            const uint32_t u = (uint32_t)(b0 + ul);
-            uint4 w[2][R];
-            float dsc[2][R];
-            uint32_t dbits[2][R];
+        // Stage body for C routed slots (compile-time), C = cnt.
+        auto stage = [&](auto cc) {
+            constexpr int C = decltype(cc)::value;
+            int tok[C];
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
+            for (int m = 0; m < C; ++m) tok[m] = list[first + m] / p.topk;
+#pragma unroll 1
+            for (int it = 0; it < UPL; ++it) {
+                const int ul = it * 32 + lane;
+                if (ul >= nb) continue;
+                const uint32_t u = (uint32_t)(b0 + ul);
+                uint4 w[R];
+                float dsc[R];
+                uint32_t dbits[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    w[s][r] = lds128(slot + (uint32_t)(((s * R + r) * nb + ul) * 16));
-                    if (p.dcopy) {
-                        uint32_t bits;
-                        asm volatile("ld.shared.u16 %0, [%1];"
-                                     : "=r"(bits)
-                                     : "r"(slot + (uint32_t)(p.d_off + ((s * R + r) * nb + ul) * 2)));
-                        dbits[s][r] = bits;
-                    } else {
-                        const uint16_t* d = s == 0 ? p.dg : p.du;
-                        dbits[s][r] = r < rv ? (uint32_t)__ldg(d + ((size_t)e * p.N + r0 + r) * p.nblk + u) : 0u;
-                    }
-                    dsc[s][r] = f16_bits_to_f32(dbits[s][r]);
+                    w[r] = lds128(qb + (uint32_t)r * QROW + (uint32_t)(it * 512));
+                    if (p.dcopy)
+                        dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
+                    else
+                        dbits[r] = r < rv ? (uint32_t)__ldg(dglob + ((size_t)e * p.N + r0 + r) * p.nblk + u) : 0u;
+                    dsc[r] = f16_bits_to_f32(dbits[r]);
                 }
-            if constexpr (PURE) {
+                if constexpr (PURE) {
 #pragma unroll
-                for (int s = 0; s < 2; ++s)
+                    for (int r = 0; r < R; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
+                } else {
+                    uint32_t xa[C];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) fold[s][r] ^= w[s][r].x ^ w[s][r].y ^ w[s][r].z ^ w[s][r].w ^ dbits[s][r];
-            } else {
-                float2 acc[2][R][kMaxC];
+                    for (int m = 0; m < C; ++m) xa[m] = xs + ((uint32_t)tok[m] * 8u * (uint32_t)U + u) * 16u;
+                    float2 acc[R][C];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    Word8 d8[2][R];
+                    for (int i = 0; i < 4; ++i) {
+                        Word8s d8[R];
 #pragma unroll
-                    for (int s = 0; s < 2; ++s)
+                        for (int r = 0; r < R; ++r)
+                            d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
+#pragma unroll
+                        for (int m = 0; m < C; ++m) {
+                            const float4 xl = lds128f(xa[m] + (uint32_t)i * qstride);
+                            const float4 xh = lds128f(xa[m] + (uint32_t)(4 + i) * qstride);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][m];
+                                a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
+                                a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
+                                a = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), a);
+                                a = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), a);
+                                acc[r][m] = a;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < C; ++m) {
+                        const float2 fa = lds64f(aux + ((uint32_t)tok[m] * (uint32_t)U + u) * 8u);
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            const uint32_t wd = i == 0 ? w[s][r].x : i == 1 ? w[s][r].y : i == 2 ? w[s][r].z : w[s][r].w;
-                            d8[s][r] = decode_word<8>(wd);
-                        }
-#pragma unroll
-                    for (int m = 0; m < kMaxC; ++m) {
-                        if (m < cnt) {
-                            const float4 xl = lds128f(xs + xs_index((uint32_t)tok[m], (uint32_t)i, u, U) * 4u);
-                            const float4 xh = lds128f(xs + xs_index((uint32_t)tok[m], (uint32_t)(4 + i), u, U) * 4u);
-#pragma unroll
-                            for (int s = 0; s < 2; ++s)
-#pragma unroll
-                                for (int r = 0; r < R; ++r) {
-                                    float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[s][r][m];
-                                    a = ffma2(d8[s][r].lo01, make_float2(xl.x, xl.y), a);
-                                    a = ffma2(d8[s][r].lo23, make_float2(xl.z, xl.w), a);
-                                    a = ffma2(d8[s][r].hi01, make_float2(xh.x, xh.y), a);
-                                    a = ffma2(d8[s][r].hi23, make_float2(xh.z, xh.w), a);
-                                    acc[s][r][m] = a;
-                                }
+                            const float t = fmaf(acc[r][m].x + acc[r][m].y, fa.x, fa.y);
+                            tot[r][m] = fmaf(dsc[r], t, tot[r][m]);
                         }
                     }
                 }
-#pragma unroll
-                for (int m = 0; m < kMaxC; ++m)
-                    if (m < cnt) {
-#pragma unroll
-                        for (int s = 0; s < 2; ++s)
-#pragma unroll
-                            for (int r = 0; r < R; ++r)
-                                tot[s][r][m] = ffma2(make_float2(dsc[s][r], dsc[s][r]), acc[s][r][m], tot[s][r][m]);
-                    }
             }
-        }
+            __syncwarp();  // every lane is done with this slot before a later stage overwrites it
 
-        __syncwarp();  // every lane is done with this slot before a later stage overwrites it
-
-        if (c == p.S - 1) {
-            if constexpr (PURE) {
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
+            if (k.c == p.S - 1) {
+                float* y = k.sp == 0 ? p.yg : p.yu;
+                if constexpr (PURE) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
 #pragma unroll
-                        for (int off = 16; off >= 1; off >>= 1)
-                            fold[s][r] ^= __shfl_xor_sync(0xffffffffu, fold[s][r], off);
-                        if (lane < cnt && r < rv) {
-                            const int slot_i = list[first + lane];
-                            (s == 0 ? p.yg : p.yu)[(size_t)slot_i * p.N + r0 + r] = __uint_as_float(fold[s][r]);
-                        }
-                        fold[s][r] = 0u;
+                        for (int off = 16; off >= 1; off >>= 1) fold[r] ^= __shfl_xor_sync(0xffffffffu, fold[r], off);
+                        if (lane < cnt && r < rv) y[(size_t)list[first + lane] * p.N + r0 + r] = __uint_as_float(fold[r]);
+                        fold[r] = 0u;
                     }
-            } else {
-                constexpr int NV = 2 * R * kMaxC;
-                constexpr int P2 = NextPow2<NV>::value;
-                constexpr int L2 = log2_const<P2>();
-                float vals[P2];
+                } else {
+                    constexpr int NV = R * C;
+                    constexpr int P2 = NextPow2<NV>::value;
+                    constexpr int L2 = log2_const<P2>();
+                    float vals[P2];
 #pragma unroll
-                for (int i = 0; i < P2; ++i) vals[i] = 0.f;
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
+                    for (int i = 0; i < P2; ++i) vals[i] = 0.f;
 #pragma unroll
                     for (int r = 0; r < R; ++r)
 #pragma unroll
-                        for (int m = 0; m < kMaxC; ++m) {
-                            vals[(s * R + r) * kMaxC + m] = tot[s][r][m].x + tot[s][r][m].y;
-                            tot[s][r][m] = make_float2(0.f, 0.f);
+                        for (int m = 0; m < C; ++m) {
+                            vals[r * C + m] = tot[r][m];
+                            tot[r][m] = 0.f;
                         }
-                warp_transpose_reduce<P2>(vals, lane);
-                const int idx = lane >> (5 - L2);
-                const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
-                if (leader && idx < NV) {
-                    const int sr = idx / kMaxC;
-                    const int m = idx - sr * kMaxC;
-                    const int s = sr / R;
-                    const int r = sr - s * R;
-                    if (r < rv && m < cnt) {
-                        const int slot_i = list[first + m];
-                        (s == 0 ? p.yg : p.yu)[(size_t)slot_i * p.N + r0 + r] = vals[0];
+                    warp_transpose_reduce<P2>(vals, lane);
+                    const int idx = lane >> (5 - L2);
+                    const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
+                    if (leader && idx < NV) {
+                        const int r = idx / C;
+                        const int m = idx - r * C;
+                        if (r < rv) y[(size_t)list[first + m] * p.N + r0 + r] = vals[0];
                     }
                 }
             }
+        };
+        if constexpr (PURE) {
+            stage(std::integral_constant<int, 1>{});
+        } else {
+            switch (cnt) {
+                case 1: stage(std::integral_constant<int, 1>{}); break;
+                case 2: stage(std::integral_constant<int, 2>{}); break;
+                case 3: stage(std::integral_constant<int, 3>{}); break;
+                default: stage(std::integral_constant<int, 4>{}); break;
+            }
         }
+        advance(k);
+        cslot = cslot + 1 == D ? 0 : cslot + 1;
     }
 }
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-void plan_override(int* cb, int* d) {
-    static int o_cb = -1, o_d = -1;
+// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth" (variant 48: 4 rows
+// x 8 warps; 216: 2 rows x 16 warps). Used for tuning sweeps; the defaults come from such sweeps.
+void plan_override(int* variant, int* depth) {
+    static int o_v = -1, o_d = -1;
     static std::once_flag once;
     std::call_once(once, [] {
         const char* e = getenv("Q4GEMV_MOE_PLAN");
-        if (e) sscanf(e, "%d,%d", &o_cb, &o_d);
+        if (e) sscanf(e, "%d,%d", &o_v, &o_d);
     });
-    if (o_cb > 0) *cb = o_cb;
-    if (o_d > 0) *d = o_d;
+    if (o_v > 0) *variant = o_v;
+    if (o_d > 0) *depth = o_d;
 }
 
 unsigned* fault_word(int device) {
@@ -423,63 +487,48 @@ unsigned* fault_word(int device) {
     return ptrs[device & 63];
 }
 
-template <int R, int W, int D, bool PURE>
-cudaError_t launch_plan(const DeviceInfo& di, const MoEParams& p, uint32_t smem, cudaStream_t s) {
+template <int R, int W, int D, int UPL, bool PURE>
+cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
+    const uint32_t route = (uint32_t)round_up(kRouteInts * 4, 128);
+    const uint32_t xsb = PURE ? 0u : (uint32_t)round_up(p.T * p.K * 4, 128);
+    const uint32_t axb = PURE ? 0u : (uint32_t)round_up(p.T * p.nblk * 8, 128);
+    p.route_off = 0;
+    p.xs_off = route;
+    p.aux_off = route + xsb;
+    p.slots_off = route + xsb + axb;
+    const uint32_t smem = p.slots_off + (uint32_t)(W * D) * moe_slot_bytes(R, UPL);
+    if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
+    p.S = (p.nblk + 32 * UPL - 1) / (32 * UPL);
+    auto kern = moe_q4_kernel<R, W, D, UPL, PURE>;
     static std::once_flag attr_once[64];
-    auto kern = moe_q4_kernel<R, W, D, PURE>;
     cudaError_t err = cudaSuccess;
     std::call_once(attr_once[di.device & 63], [&] {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
     });
     if (err != cudaSuccess) return err;
-    // worst case: every slot its own group
-    const long long max_jobs = (long long)(p.T * p.topk) * ((p.N + R - 1) / R);
-    const int grid = (int)std::min<long long>(di.sm_count, std::max<long long>(1, max_jobs));
-    kern<<<grid, W * 32, smem, s>>>(p);
+    kern<<<di.sm_count, W * 32, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-// Shared memory: [routing tables][staged inputs T*K*4][W rings of D slots]; chunk and depth shrink until
-// it fits.
+template <int R, int W, int UPL, bool PURE>
+cudaError_t launch_upl(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
+    cudaError_t e = cudaErrorNotSupported;
+    if (depth >= 4) e = launch_fixed<R, W, 4, UPL, PURE>(di, p, s);
+    if (e == cudaErrorNotSupported && depth >= 3) e = launch_fixed<R, W, 3, UPL, PURE>(di, p, s);
+    if (e == cudaErrorNotSupported) e = launch_fixed<R, W, 2, UPL, PURE>(di, p, s);
+    return e;
+}
+
+// Whole rows in one chunk up to K = 4096 (UPL = 1, 2, 4), longer rows in 128-block chunks; the deepest ring
+// that fits beside the routing tables and the staged tokens.
 template <int R, int W, bool PURE>
-cudaError_t run(const DeviceInfo& di, MoEParams p, int CB, int D, cudaStream_t s) {
-    plan_override(&CB, &D);
-    D = std::max(2, std::min(4, D));
-    const bool dcopy = (p.nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.dg) & 15u) == 0) &&
-                       ((reinterpret_cast<uintptr_t>(p.du) & 15u) == 0);
-    bool ok = false;
-    uint32_t smem = 0;
-    int depth = D;
-    for (int dd = D; dd >= 2 && !ok; --dd) {
-        for (int cb0 = CB; cb0 >= 8 && !ok; cb0 /= 2) {
-            const int cb = std::min(round_up(cb0, 8), round_up(p.nblk, 8));
-            const int d_off = 2 * R * cb * 16;
-            const int slot = round_up(d_off + round_up(2 * R * cb * 2, 16), 128);
-            const uint32_t route = (uint32_t)round_up(kRouteInts * 4, 128);
-            const uint32_t xs_bytes = PURE ? 0u : (uint32_t)(p.T * p.K * 4);
-            p.route_off = 0;
-            p.xs_off = route;
-            p.slots_off = p.xs_off + xs_bytes;
-            smem = p.slots_off + (uint32_t)(W * dd * slot);
-            if (smem <= (uint32_t)di.max_smem_optin) {
-                ok = true;
-                p.CB = cb;
-                p.d_off = d_off;
-                p.slot_bytes = slot;
-                depth = dd;
-            }
-        }
-    }
-    if (!ok) return cudaErrorNotSupported;
-    p.dcopy = dcopy ? 1 : 0;
-    p.S = (p.nblk + p.CB - 1) / p.CB;
-    p.fault = fault_word(di.device);
-    if (!p.fault) return cudaErrorInvalidSymbol;
-    switch (depth) {
-        case 2: return launch_plan<R, W, 2, PURE>(di, p, smem, s);
-        case 3: return launch_plan<R, W, 3, PURE>(di, p, smem, s);
-        default: return launch_plan<R, W, 4, PURE>(di, p, smem, s);
-    }
+cudaError_t launch(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
+    cudaError_t e = cudaErrorNotSupported;
+    if (p.nblk <= 32) e = launch_upl<R, W, 1, PURE>(di, p, depth, s);
+    else if (p.nblk <= 64) e = launch_upl<R, W, 2, PURE>(di, p, depth, s);
+    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 4, PURE>(di, p, depth, s);
+    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 1, PURE>(di, p, depth, s);
+    return e;
 }
 
 }  // namespace
@@ -507,8 +556,14 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.N = N;
     p.K = K;
     p.nblk = K / 32;
-    if (pure_read) return run<2, 8, true>(di, p, 64, 2, s);
-    return run<2, 8, false>(di, p, 64, 2, s);
+    p.dcopy = (p.nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(d_gate) & 15u) == 0) &&
+              ((reinterpret_cast<uintptr_t>(d_up) & 15u) == 0);
+    p.fault = fault_word(di.device);
+    if (!p.fault) return cudaErrorInvalidSymbol;
+    int variant = 48, depth = 3;
+    plan_override(&variant, &depth);
+    if (pure_read) return variant == 216 ? launch<2, 16, true>(di, p, depth, s) : launch<4, 8, true>(di, p, depth, s);
+    return variant == 216 ? launch<2, 16, false>(di, p, depth, s) : launch<4, 8, false>(di, p, depth, s);
 }
 
 cudaError_t read_and_clear_fault_moe(unsigned* out) {

@@ -153,6 +153,23 @@ int q4k_dequant(float *W, const uint8_t *w, int N, int K, q4_stream_t stream);
 const char *q4_last_error(void);
 
 /*
+ * Launch overlap (programmatic dependent launch; no counterpart in the source pages, which launch each
+ * kernel on its own). Off by default. When on, every GEMV, fused and MoE call (not the dequant dumps) is
+ * launched so that it may start while the kernel before it in the same stream is still running: the Q4
+ * and Q4_K kernels issue their first weight copies at once, then wait for that kernel's completion (and
+ * the visibility of its writes) before they read x, gamma or expert ids or write any output; the MoE kernel
+ * waits before it reads the expert ids. So a chain of calls where each x is the previous output stays
+ * exact, and each call's weight streaming overlaps the previous call's tail.
+ * Requirement while it is on: the kernel that runs directly before a call in the same stream must not
+ * write that call's weight bytes (qs, d or the Q4_K blocks); weights written earlier in the stream, or on
+ * another stream with ordinary event or stream synchronisation, are fine.
+ * The setting is process-wide and read at each launch (a CUDA graph keeps the launches it captured).
+ * q4_set_launch_overlap returns Q4_OK; q4_get_launch_overlap returns the current setting (0 or 1).
+ */
+int q4_set_launch_overlap(int enable);
+int q4_get_launch_overlap(void);
+
+/*
  * Synchronises the current device, then ORs the fault bits every kernel family recorded since the last
  * call into *faults and clears them. Returns Q4_OK or Q4_ECUDA.
  */

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
     "moe_q4_gemv", "q4_pure_read", "q4k_pure_read", "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
-    "q4_device_faults", "FAULT_BAD_EXPERT",
+    "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "FAULT_BAD_EXPERT",
 ]
 
 Q4_OK, Q4_EINVAL, Q4_EALIGN, Q4_ECUDA, Q4_EUNSUPPORTED = 0, -1, -2, -3, -4
@@ -74,6 +74,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.q4_last_error.argtypes = []
         L.q4_last_error.restype = ctypes.c_char_p
+        L.q4_set_launch_overlap.argtypes = [ctypes.c_int]
+        L.q4_set_launch_overlap.restype = ctypes.c_int
+        L.q4_get_launch_overlap.argtypes = []
+        L.q4_get_launch_overlap.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -210,6 +214,19 @@ def q4k_dequant(W, w, stream=None) -> None:
     if W.numel() != N * K:
         raise ValueError("W must be [N, K]")
     _check(load().q4k_dequant(_ptr(W, torch.float32, "W"), _ptr(w, torch.uint8, "w"), N, K, _stream(stream)))
+
+
+def q4_set_launch_overlap(enable: bool) -> None:
+    """Turn launch overlap (programmatic dependent launch) on or off for every later GEMV/MoE launch.
+
+    While on, the kernel that runs directly before a call in the same stream must not write that call's
+    weights; inputs and outputs may depend on it freely (each kernel waits for it before touching them).
+    """
+    _check(load().q4_set_launch_overlap(1 if enable else 0))
+
+
+def q4_get_launch_overlap() -> bool:
+    return bool(load().q4_get_launch_overlap())
 
 
 def q4_device_faults() -> int:

@@ -1,5 +1,6 @@
 // The C ABI: argument validation (before any CUDA call, so refusals need no GPU), the device check,
 // error reporting and dispatch to the kernel families.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -91,6 +92,12 @@ int finish(const char* what, cudaError_t e) {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_launch_overlap{0};
+}  // namespace
+
+bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
 
 cudaError_t current_device_info(DeviceInfo* out) {
     static DeviceInfo cache[64];
@@ -250,6 +257,13 @@ int q4k_dequant(float* W, const uint8_t* w, int N, int K, q4_stream_t stream) {
 }
 
 const char* q4_last_error(void) { return g_last_error.c_str(); }
+
+int q4_set_launch_overlap(int enable) {
+    g_launch_overlap.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return Q4_OK;
+}
+
+int q4_get_launch_overlap(void) { return g_launch_overlap.load(std::memory_order_relaxed); }
 
 int q4_device_faults(unsigned* faults) {
     const char* what = "q4_device_faults";

@@ -48,6 +48,12 @@ __device__ __forceinline__ void warp_copy_async(uint32_t dst, const void* src, u
                      : "memory");
 }
 
+// Programmatic dependent launch. grid_dependency_wait blocks until the grid that precedes this one in the
+// stream has completed and its writes are visible; grid_launch_dependents lets the grid that follows be
+// scheduled. Both are no-ops for a grid launched without a programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's commit groups are still in flight.

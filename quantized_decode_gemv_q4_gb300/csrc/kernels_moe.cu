@@ -52,14 +52,22 @@ struct MoEParams {
     int32_t* status;
     int T, topk, E, N, K, nblk;
     int S, dcopy;
+    int cost_a, cost_b;
     uint32_t route_off, xs_off, aux_off, slots_off;
     unsigned* fault;
 };
 
 // Routing tables in shared memory (route_off): slot_ids[kMaxSlots], rank[kMaxSlots], owner[kMaxSlots],
 // ucount[kMaxSlots], uoffset[kMaxSlots+1], list[kMaxSlots], group_ux[kMaxSlots], group_first[kMaxSlots],
-// group_cnt[kMaxSlots], scalars[4] (number of distinct experts, number of groups).
-constexpr int kRouteInts = 9 * kMaxSlots + 8;
+// group_cnt[kMaxSlots], scalars[4] (number of distinct experts, number of groups), then the cumulative job
+// cost gcum[kMaxSlots+1] (64-bit) and the job order of the groups gorder[kMaxSlots] (groups sorted by slot
+// count).
+constexpr int kRouteInts = 9 * kMaxSlots + 8 + 2 * (kMaxSlots + 1) + 2 + kMaxSlots;
+
+// Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
+// (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
+// routings with 1, 2 and 4 slots per expert). The pure-read instrument costs the same for every C.
+__device__ __forceinline__ long long job_cost(int C, bool pure, int a, int b) { return pure ? 1 : a + (long long)b * C; }
 
 __host__ __device__ constexpr uint32_t moe_slot_bytes(int R, int UPL) {
     return (uint32_t)(((R * 32 * UPL * 18) + 127) / 128 * 128);
@@ -94,6 +102,13 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     int* group_first = route + 7 * kMaxSlots + 1;
     int* group_cnt = route + 8 * kMaxSlots + 1;
     int* scalars = route + 9 * kMaxSlots + 1;
+    long long* gcum = reinterpret_cast<long long*>(route + 9 * kMaxSlots + 8);  // 8-byte aligned
+    int* gorder = route + 9 * kMaxSlots + 8 + 2 * (kMaxSlots + 1) + 2;
+
+    // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
+    // in the stream (it may have written ids, x or the outputs) before anything else.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     // ---- routing -------------------------------------------------------------------------------------
     for (int i = threadIdx.x; i < TK; i += kThreads) {
@@ -207,11 +222,53 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
     const int jobs = ngroups * 2 * rgs;
-    const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
+    // Warps are numbered CTA by CTA, and the groups run in order of slot count, so the warps of one SM own
+    // neighbouring job ranges and mostly run the same compiled stage body (one set of instructions hot).
+    const int gw = (int)blockIdx.x * W + warp;
     const int Wtot = (int)gridDim.x * W;
-    // this warp's contiguous range of jobs [j0, j1)
-    const int j0 = (int)(((long long)jobs * gw) / Wtot);
-    const int j1 = (int)(((long long)jobs * (gw + 1)) / Wtot);
+    // Job order of the groups (stable by slot count), then the cumulative cost in that order (each group has
+    // 2 * rgs jobs of cost job_cost(cnt)), then this warp's share of the total cost as a contiguous job range
+    // [j0, j1): groups with more routed slots spread over more warps.
+    if (warp == 0) {
+        int base = 0;
+        for (int c = 1; c <= kMaxC; ++c) {
+            for (int c0 = 0; c0 < ngroups; c0 += 32) {
+                const int gi = c0 + lane;
+                const bool mine = gi < ngroups && (group_cnt[gi] & 0xFF) == c;
+                const unsigned mb = __ballot_sync(0xffffffffu, mine);
+                if (mine) gorder[base + __popc(mb & ((1u << lane) - 1u))] = gi;
+                base += __popc(mb);
+            }
+        }
+        __syncwarp();
+        long long cb = 0;
+        for (int c0 = 0; c0 < ngroups; c0 += 32) {
+            const int oi = c0 + lane;
+            long long v = oi < ngroups ? 2LL * rgs * job_cost(group_cnt[gorder[oi]] & 0xFF, PURE, p.cost_a, p.cost_b) : 0LL;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long t = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += t;
+            }
+            if (oi < ngroups) gcum[oi + 1] = cb + v;
+            cb += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) gcum[0] = 0;
+    }
+    __syncthreads();
+    const long long total_cost = gcum[ngroups];
+    auto job_at = [&](long long c) {  // the job that holds cost offset c
+        if (c >= total_cost) return jobs;
+        int lo = 0, hi = ngroups - 1;  // largest g with gcum[g] <= c
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gcum[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo * 2 * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]] & 0xFF, PURE, p.cost_a, p.cost_b));
+    };
+    const int j0 = job_at(total_cost * gw / Wtot);
+    const int j1 = job_at(total_cost * (gw + 1) / Wtot);
     const uint64_t pol = policy_evict_first();
 
     // Job cursor: group, projection, row group, chunk. Jobs run group-major, then projection, then row
@@ -246,7 +303,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     int issued = 0, islot = 0;
     auto issue = [&]() {
         if (issued < total) {
-            const int e = group_cnt[ik.grp] >> 8;
+            const int e = group_cnt[gorder[ik.grp]] >> 8;
             const int r0 = ik.rg * R;
             const int rv = min(R, p.N - r0);
             const int b0 = ik.c * CB;
@@ -333,10 +390,11 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         cp_async_wait<D - 1>();  // stage g has landed
         __syncwarp();
         const uint32_t slot = ring + (uint32_t)cslot * SLOT;
-        const int gc = group_cnt[k.grp];
+        const int grp = gorder[k.grp];
+        const int gc = group_cnt[grp];
         const int cnt = gc & 0xFF;
         const int e = gc >> 8;
-        const int first = group_first[k.grp];
+        const int first = group_first[grp];
         const int r0 = k.rg * R;
         const int rv = min(R, p.N - r0);
         const int b0 = k.c * CB;
@@ -462,17 +520,20 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth" (variant 48: 4 rows
-// x 8 warps; 216: 2 rows x 16 warps). Used for tuning sweeps; the defaults come from such sweeps.
-void plan_override(int* variant, int* depth) {
-    static int o_v = -1, o_d = -1;
+// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b"
+// (variant 48: 4 rows x 8 warps; 216: 2 rows x 16 warps; job cost cost_a + cost_b * C). Used for tuning
+// sweeps; the defaults come from such sweeps.
+void plan_override(int* variant, int* depth, int* cost_a, int* cost_b) {
+    static int o_v = -1, o_d = -1, o_a = -1, o_b = -1;
     static std::once_flag once;
     std::call_once(once, [] {
         const char* e = getenv("Q4GEMV_MOE_PLAN");
-        if (e) sscanf(e, "%d,%d", &o_v, &o_d);
+        if (e) sscanf(e, "%d,%d,%d,%d", &o_v, &o_d, &o_a, &o_b);
     });
     if (o_v > 0) *variant = o_v;
     if (o_d > 0) *depth = o_d;
+    if (o_a > 0) *cost_a = o_a;
+    if (o_b > 0) *cost_b = o_b;
 }
 
 unsigned* fault_word(int device) {
@@ -506,8 +567,7 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
     });
     if (err != cudaSuccess) return err;
-    kern<<<di.sm_count, W * 32, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, di.sm_count, W * 32, smem, s, p);
 }
 
 template <int R, int W, int UPL, bool PURE>
@@ -561,7 +621,9 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.fault = fault_word(di.device);
     if (!p.fault) return cudaErrorInvalidSymbol;
     int variant = 48, depth = 3;
-    plan_override(&variant, &depth);
+    p.cost_a = 9;
+    p.cost_b = 5;
+    plan_override(&variant, &depth, &p.cost_a, &p.cost_b);
     if (pure_read) return variant == 216 ? launch<2, 16, true>(di, p, depth, s) : launch<4, 8, true>(di, p, depth, s);
     return variant == 216 ? launch<2, 16, false>(di, p, depth, s) : launch<4, 8, false>(di, p, depth, s);
 }

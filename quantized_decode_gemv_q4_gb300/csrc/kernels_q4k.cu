@@ -96,6 +96,10 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
 
     for (int g = 0; g < D - 1; ++g) issue(g);
 
+    // The weights are constant; x, gamma and the outputs may belong to the previous kernel in the stream.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
     if constexpr (!PURE) {
         const int K4 = p.K >> 2;
         float r = 1.0f;
@@ -389,8 +393,7 @@ cudaError_t launch_plan(const DeviceInfo& di, Q4KParams p, uint32_t smem, cudaSt
     });
     if (err != cudaSuccess) return err;
     const int grid = std::min(di.sm_count, p.jobs);
-    kern<<<grid, W * 32, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, W * 32, smem, s, p);
 }
 
 // Shared memory: [staged xhat K*4][sub-block sums K/32*4][W reduction floats][W header tables]

@@ -17,6 +17,26 @@ struct DeviceInfo {
 // Cached per-device properties of the current device (thread-safe after first call).
 cudaError_t current_device_info(DeviceInfo* out);
 
+// Process-wide launch-overlap setting (programmatic dependent launch), set through the C ABI.
+bool launch_overlap();
+
+// Launch a GEMV kernel; with launch overlap on, it may start while the previous kernel in the stream is
+// still running (the kernel waits for it before touching inputs or outputs, see grid_dependency_wait).
+template <typename Kernel, typename Params>
+cudaError_t launch_kernel(Kernel kern, int grid, int block, uint32_t smem, cudaStream_t s, const Params& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_overlap() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 // ---- planar Q4 (32-weight blocks, f16 scale per block) -------------------------------------------
 // Y[v][n] = sum_k W[n][k] * X[v][k] for v < V; V in 1..8. Returns cudaErrorNotSupported when the
 // staged input does not fit in shared memory.

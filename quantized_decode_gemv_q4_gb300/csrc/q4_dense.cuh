@@ -115,6 +115,10 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
 #pragma unroll
     for (int k = 0; k < D - 1; ++k) issue();
 
+    // The weights are constant; the input and the outputs may belong to the previous kernel in the stream.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
     if constexpr (!PURE) {
         // Stage the V vectors (X is [V][K]): each thread takes whole 32-element blocks, issues the eight
         // float4 loads of kStageB blocks before using any, sums each block and finds its largest magnitude
@@ -368,8 +372,7 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     p.aux_off = xsb;
     p.slots_off = xsb + axb;
     const int grid = std::min(di.sm_count, p.jobs);
-    kern<<<grid, W * 32, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, W * 32, smem, s, p);
 }
 
 // The deepest ring among the instantiated depths {2, 3, 4, 5, 6, 8} not above DMAX nor `want` that fits.

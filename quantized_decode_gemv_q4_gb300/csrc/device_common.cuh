@@ -222,6 +222,41 @@ __device__ __forceinline__ float stage_scaled(float x, int hi, uint32_t jj, int 
 // or more are outside the supported range and yield a non-finite result).
 __device__ __forceinline__ float block_factor(int e) { return 22 + e <= 127 ? pow2i(22 + e) : INFINITY; }
 
+// Four lanes stage one 32-element block: lane t of an aligned group of 4 holds float4 2t and 2t+1 (both in
+// the same half: elements 8t .. 8t+7). The group's sum and largest magnitude (fixed tree), then every lane
+// scales its eight elements with the block's exponent bound e for code positions (hi, jj): the staged value
+// is x * 2^(127-p-e), applied as two exact power-of-two factors per position.
+struct Stage4 {
+    float sum;  // block sum (every lane of the group)
+    int e;      // exponent bound
+    float4 a, b;  // the lane's two float4, scaled
+};
+__device__ __forceinline__ Stage4 stage_block4(float4 a, float4 b, int hi) {
+    Stage4 st;
+    float s = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+    float m = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                    fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    st.sum = s;
+    st.e = block_exponent(m);
+    float f1[4], f2[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const int p = hi ? (jj == 0 ? 4 : jj == 1 ? 12 : jj == 2 ? 8 : 16) : (jj == 0 ? 0 : jj == 1 ? 8 : jj == 2 ? 16 : 12);
+        const int k = 127 - p - st.e;
+        const int k1 = k >> 1;
+        f1[jj] = pow2i(k1);
+        f2[jj] = pow2i(k - k1);
+    }
+    st.a = make_float4((a.x * f1[0]) * f2[0], (a.y * f1[1]) * f2[1], (a.z * f1[2]) * f2[2], (a.w * f1[3]) * f2[3]);
+    st.b = make_float4((b.x * f1[0]) * f2[0], (b.y * f1[1]) * f2[1], (b.z * f1[2]) * f2[2], (b.w * f1[3]) * f2[3]);
+    return st;
+}
+
+
 // Sum and largest magnitude of 32 consecutive elements held as one float4 by each of 8 aligned lanes; every
 // lane of the group gets both (fixed summation tree).
 __device__ __forceinline__ void block8_sum_max(const float4& v, float& sum, float& mx) {

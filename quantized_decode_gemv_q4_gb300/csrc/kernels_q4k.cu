@@ -6,17 +6,21 @@
 // lives in chunk c = e/64: low nibbles of the chunk's 32 bytes are sub-block 2c, high nibbles sub-block 2c+1;
 // its value is d*sc_j*q - dmin*m_j for its sub-block j.
 //
-// Kernel shape (one CTA of W warps per SM, persistent), as the planar Q4 kernels:
-//  * prologue: every warp issues its first weight copies, then the CTA computes sum(x^2) (block reduction),
-//    r = rsqrt(sum/K + eps) and xhat = x * r * gamma, which it keeps in shared memory only (permuted and
-//    pre-scaled per nibble position), together with the 32-element sub-block sums S_j of xhat;
-//  * each warp streams R rows of each of NS weight matrices through its own ring of cp.async slots;
-//  * per slot, the warp first decodes each super-block header once: d*sc_j into a small table, and the
-//    whole min term dmin * sum_j m_j * S_j straight into its row accumulators;
+// Kernel shape (one persistent CTA of W warps per SM):
+//  * prologue: every warp issues its first weight copies; after the previous kernel in the stream is done
+//    the CTA computes sum(x^2) (block reduction), r = rsqrt(sum/K + eps) and xhat = x * r * gamma, which it
+//    keeps in shared memory only: each 32-element sub-block j is staged pre-scaled with its own exponent
+//    bound e_j (the bias-free decode of device_common.cuh), next to (S_j = sum of xhat over j, 2^(22+e_j));
+//  * each warp streams R rows of each of NS weight matrices (whole rows when they fit) through its own ring
+//    of cp.async slots, with incremental per-stage control;
+//  * per slot, the warp first decodes each super-block header once: d*sc_j*2^(22+e_j) into a small table
+//    (so the unit loop needs no per-block factor), and the whole min term dmin * sum_j m_j * S_j straight
+//    into its row accumulators;
 //  * then lane l takes 16-byte quant unit l (+32, ...): chunk c = (l%8)/2, half h = l%2 of a super-block,
-//    i.e. 16 codes of sub-block 2c and 16 of 2c+1, all against the same 32 staged inputs, and folds them
-//    with d*sc_2c and d*sc_2c+1 from the table;
+//    i.e. 16 codes of sub-block 2c and 16 of 2c+1 against the same 32 staged inputs: one shift and eight
+//    ANDs per word, packed fp32x2 FMAs into one accumulator per sub-block, folded with the table entries;
 //  * row totals are summed over the warp and stored. The NS matrices share every staged-input load.
+// Inputs whose staged value reaches 2^83 in magnitude are outside the supported range (non-finite result).
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -38,13 +42,18 @@ struct Q4KParams {
     const float* gamma;  // nullptr: no RMSNorm
     float eps;
     int N, K, nsb;
-    int CS;          // super-blocks per chunk
-    int S;           // chunks per row
-    int jobs;        // row groups of R rows (per stream)
-    int slot_bytes;  // multiple of 128
-    int table_bytes; // per warp
+    int CS;           // super-blocks per chunk
+    int S;            // chunks per row
+    int jobs;         // row groups of R rows (per stream)
+    int slot_bytes;   // multiple of 128
+    int table_bytes;  // per warp
     uint32_t xs_off, ssum_off, red_off, tables_off, slots_off;
 };
+
+// byte j of w as an exact float (0x4B000000 | b is 2^23 + b)
+__device__ __forceinline__ float byte_as_float(uint32_t w, int j) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + (uint32_t)j)) - 8388608.0f;
+}
 
 template <int NS, int R, int W, int D, bool PURE>
 __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) {
@@ -59,25 +68,23 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
     const uint32_t ssum = s_base + p.ssum_off;
     const uint32_t red = s_base + p.red_off;
     const uint32_t table = s_base + p.tables_off + (uint32_t)(warp * p.table_bytes);
-    const uint32_t slots = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
+    const uint32_t ring = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
 
+    // Warps are numbered across CTAs first so that a small job count still spreads over all SMs.
     const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
     const int Wtot = (int)gridDim.x * W;
-    const int my_jobs = gw < p.jobs ? (p.jobs - 1 - gw) / Wtot + 1 : 0;
-    const int total = my_jobs * p.S;
     const uint64_t pol = policy_evict_first();
     const size_t row_bytes = (size_t)p.nsb * 144;
 
-    // Stage g of this warp -> slot g % D; one commit group per stage (empty when g >= total).
-    auto issue = [&](int g) {
-        if (g < total) {
-            const int job = gw + (g / p.S) * Wtot;
-            const int c = g % p.S;
-            const int r0 = job * R;
+    // Issue pointer (job, chunk, slot); one commit group per call, empty once this warp has nothing left.
+    int ijob = gw, ic = 0, islot = 0;
+    auto issue = [&]() {
+        if (ijob < p.jobs) {
+            const int r0 = ijob * R;
             const int rv = min(R, p.N - r0);
-            const int sb0 = c * p.CS;
+            const int sb0 = ic * p.CS;
             const int cs = min(p.CS, p.nsb - sb0);
-            const uint32_t slot = slots + (uint32_t)((g % D) * p.slot_bytes);
+            const uint32_t slot = ring + (uint32_t)(islot * p.slot_bytes);
 #pragma unroll
             for (int s = 0; s < NS; ++s) {
                 const uint8_t* src = (s == 0 ? p.w0 : p.w1) + (size_t)r0 * row_bytes + (size_t)sb0 * 144;
@@ -90,11 +97,17 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
                                         (uint32_t)(cs * 144), lane, pol);
                 }
             }
+            if (++ic == p.S) {
+                ic = 0;
+                ijob += Wtot;
+            }
+            islot = islot + 1 == D ? 0 : islot + 1;
         }
         cp_async_commit();
     };
 
-    for (int g = 0; g < D - 1; ++g) issue(g);
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue();
 
     // The weights are constant; x, gamma and the outputs may belong to the previous kernel in the stream.
     grid_dependency_wait();
@@ -104,14 +117,22 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
         const int K4 = p.K >> 2;
         float r = 1.0f;
         if (p.gamma) {
-            // sum of squares over K: per-thread partials, warp shuffles, then one value per warp
+            // sum of squares over K: per-thread partials (loads issued ahead), warp shuffles, one value per warp
             float ss = 0.f;
-            for (int idx = threadIdx.x; idx < K4; idx += kThreads) {
-                const float4 xv = __ldg(reinterpret_cast<const float4*>(p.x) + idx);
-                ss = fmaf(xv.x, xv.x, ss);
-                ss = fmaf(xv.y, xv.y, ss);
-                ss = fmaf(xv.z, xv.z, ss);
-                ss = fmaf(xv.w, xv.w, ss);
+            for (int base = threadIdx.x; base < K4; base += kThreads * kStageU) {
+                float4 xv[kStageU];
+#pragma unroll
+                for (int j = 0; j < kStageU; ++j) {
+                    const int idx = base + j * kThreads;
+                    xv[j] = idx < K4 ? __ldg(reinterpret_cast<const float4*>(p.x) + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < kStageU; ++j) {
+                    ss = fmaf(xv[j].x, xv[j].x, ss);
+                    ss = fmaf(xv[j].y, xv[j].y, ss);
+                    ss = fmaf(xv[j].z, xv[j].z, ss);
+                    ss = fmaf(xv[j].w, xv[j].w, ss);
+                }
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -122,33 +143,40 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
             for (int w = 0; w < W; ++w) tot += lds32f(red + (uint32_t)w * 4u);
             r = rsqrtf(tot / (float)p.K + p.eps);
         }
-        // xhat = (x * r) * gamma, staged permuted and pre-scaled; S_j = sum of xhat over sub-block j.
-        // A warp covers 32 consecutive float4 = 4 whole sub-blocks, and K/4 is a multiple of 64, so every
-        // lane of a warp takes the same number of trips and the 8-lane shuffles below are complete.
-        for (int idx = threadIdx.x; idx < K4; idx += kThreads) {
-            const uint32_t k = (uint32_t)idx * 4u;
-            float4 xv = __ldg(reinterpret_cast<const float4*>(p.x) + idx);
+        // xhat = (x * r) * gamma, four lanes per 32-element sub-block (lane t of the group holds float4 2t,
+        // 2t+1): the group's sum S_j and largest magnitude, then the block staged pre-scaled with its exponent
+        // bound e_j. Sub-block j = 8*sb + 2c + k holds the low (k = 0) or high (k = 1) codes of units
+        // 8*sb + 2c + h, h = element/16; its float4 f lands in quad 4k + f%4 of unit 8*sb + 2c + f/4.
+        // K/32 is a multiple of 8, so whole warps take part in every group shuffle.
+        const int nsub = p.K / 32;
+        const int t4 = lane & 3;
+        for (int thr = threadIdx.x; thr < nsub * 4; thr += kThreads) {
+            const int js = thr >> 2;
+            const float4* src = reinterpret_cast<const float4*>(p.x) + js * 8 + 2 * t4;
+            float4 xa = __ldg(src), xb = __ldg(src + 1);
             if (p.gamma) {
-                const float4 gv = __ldg(reinterpret_cast<const float4*>(p.gamma) + idx);
-                xv.x = (xv.x * r) * gv.x;
-                xv.y = (xv.y * r) * gv.y;
-                xv.z = (xv.z * r) * gv.z;
-                xv.w = (xv.w * r) * gv.w;
+                const float4* gsrc = reinterpret_cast<const float4*>(p.gamma) + js * 8 + 2 * t4;
+                const float4 ga = __ldg(gsrc), gb = __ldg(gsrc + 1);
+                xa = make_float4((xa.x * r) * ga.x, (xa.y * r) * ga.y, (xa.z * r) * ga.z, (xa.w * r) * ga.w);
+                xb = make_float4((xb.x * r) * gb.x, (xb.y * r) * gb.y, (xb.z * r) * gb.z, (xb.w * r) * gb.w);
             }
-            float part = (xv.x + xv.y) + (xv.z + xv.w);
-            part += __shfl_xor_sync(0xffffffffu, part, 4);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            if ((lane & 7) == 0)
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(ssum + (k >> 5) * 4u), "f"(part) : "memory");
-            uint32_t u, q, jj;
-            int hi;
-            q4k_elem_place(k, u, q, jj, hi);
-            const uint32_t a = xs + xs_index(0u, q, u, U) * 4u;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(xv.x * pos_scale_dev(hi, 0)),
-                         "f"(xv.y * pos_scale_dev(hi, 1)), "f"(xv.z * pos_scale_dev(hi, 2)),
-                         "f"(xv.w * pos_scale_dev(hi, 3))
+            const int k = js & 1;
+            const Stage4 st = stage_block4(xa, xb, k);
+            const uint32_t ubase = (uint32_t)(js & ~1);  // 8*sb + 2c
+            const int f0 = 2 * t4;                        // float4 index of xa inside the sub-block
+            const uint32_t u = ubase + (uint32_t)(f0 >> 2);
+            const uint32_t q0 = (uint32_t)(4 * k + (f0 & 3));
+            const uint32_t a0 = xs + xs_index(0u, q0, u, U) * 4u;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y), "f"(st.a.z),
+                         "f"(st.a.w)
                          : "memory");
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + U * 16u), "f"(st.b.x), "f"(st.b.y),
+                         "f"(st.b.z), "f"(st.b.w)
+                         : "memory");
+            if (t4 == 0)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ssum + (uint32_t)js * 8u), "f"(st.sum),
+                             "f"(block_factor(st.e))
+                             : "memory");
         }
     }
     __syncthreads();
@@ -166,67 +194,81 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
         }
 
     const uint32_t cpos = (uint32_t)(lane & 7);  // unit position inside a super-block: chunk cpos/2, half cpos%2
-
+    const int my_jobs = gw < p.jobs ? (p.jobs - 1 - gw) / Wtot + 1 : 0;
+    const int total = my_jobs * p.S;
+    int job = gw, c = 0, cslot = 0;
     for (int g = 0; g < total; ++g) {
-        issue(g + D - 1);
-        cp_async_wait<D - 1>();
+        issue();                 // stage g + D - 1 into the slot consumed at g - 1
+        cp_async_wait<D - 1>();  // stage g has landed
         __syncwarp();
-        const uint32_t slot = slots + (uint32_t)((g % D) * p.slot_bytes);
-
-        const int job = gw + (g / p.S) * Wtot;
-        const int c = g % p.S;
+        const uint32_t slot = ring + (uint32_t)(cslot * p.slot_bytes);
         const int r0 = job * R;
         const int rv = min(R, p.N - r0);
         const int sb0 = c * p.CS;
         const int cs = min(p.CS, p.nsb - sb0);
+        const int nitems = NS * R * cs;
 
-        // 1) headers: one lane per (stream, row, super-block)
-        for (int t = lane; t < NS * R * cs; t += 32) {
-            const int sr = t / cs;  // stream * R + row
-            const int sbl = t - sr * cs;
-            const uint4 hdr = lds128(slot + (uint32_t)((sr * cs + sbl) * 144));
-            if constexpr (PURE) {
+        // 1) headers: one lane per (stream, row, super-block) item; sr = item / cs, kept incrementally
+        {
+            int sr = 0, sbl = lane;
+            while (sbl >= cs && sr < NS * R) {
+                sbl -= cs;
+                ++sr;
+            }
+            for (int t = lane; t < nitems; t += 32) {
+                const uint4 hdr = lds128(slot + (uint32_t)(t * 144));
+                if constexpr (PURE) {
 #pragma unroll
-                for (int s = 0; s < NS; ++s)
+                    for (int s = 0; s < NS; ++s)
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        if (s * R + r == sr) fold[s][r] ^= hdr.x ^ hdr.y ^ hdr.z ^ hdr.w;
-            } else {
-                const float d = f16_bits_to_f32(hdr.x);
-                const float dmin = f16_bits_to_f32(hdr.x >> 16);
-                const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu;
-                const uint32_t m_lo = hdr.z & 0x3F3F3F3Fu;
-                const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-                const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-                const uint32_t sg = (uint32_t)(sb0 + sbl) * 8u;  // first sub-block index in the row
-                const float4 s0 = lds128f(ssum + sg * 4u);
-                const float4 s1 = lds128f(ssum + sg * 4u + 16u);
-                float dsc[8];
-                float msum = 0.f;
+                        for (int rr = 0; rr < R; ++rr)
+                            if (s * R + rr == sr) fold[s][rr] ^= hdr.x ^ hdr.y ^ hdr.z ^ hdr.w;
+                } else {
+                    const float d = f16_bits_to_f32(hdr.x);
+                    const float dmin = f16_bits_to_f32(hdr.x >> 16);
+                    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu;
+                    const uint32_t m_lo = hdr.z & 0x3F3F3F3Fu;
+                    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+                    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+                    const uint32_t sg = (uint32_t)(sb0 + sbl) * 8u;  // first sub-block index in the row
+                    float f[8], sm[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    dsc[j] = d * (float)((sc_lo >> (8 * j)) & 0xFFu);
-                    dsc[j + 4] = d * (float)((sc_hi >> (8 * j)) & 0xFFu);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 pr = lds128f(ssum + (sg + 2u * (uint32_t)q) * 8u);  // (S, 2^(22+e)) x 2
+                        sm[2 * q] = pr.x;
+                        f[2 * q] = pr.y;
+                        sm[2 * q + 1] = pr.z;
+                        f[2 * q + 1] = pr.w;
+                    }
+                    float msum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        msum = fmaf(byte_as_float(m_lo, j), sm[j], msum);
+                        msum = fmaf(byte_as_float(m_hi, j), sm[j + 4], msum);
+                    }
+#pragma unroll
+                    for (int s = 0; s < NS; ++s)
+#pragma unroll
+                        for (int rr = 0; rr < R; ++rr)
+                            if (s * R + rr == sr) mins[s][rr] = fmaf(dmin, msum, mins[s][rr]);
+                    float dsc[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        dsc[j] = (d * byte_as_float(sc_lo, j)) * f[j];
+                        dsc[j + 4] = (d * byte_as_float(sc_hi, j)) * f[j + 4];
+                    }
+                    const uint32_t te = table + (uint32_t)(t * 64);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(te + (uint32_t)cc * 16u),
+                                     "f"(dsc[2 * cc]), "f"(dsc[2 * cc]), "f"(dsc[2 * cc + 1]), "f"(dsc[2 * cc + 1])
+                                     : "memory");
                 }
-                msum = fmaf((float)(m_lo & 0xFFu), s0.x, msum);
-                msum = fmaf((float)((m_lo >> 8) & 0xFFu), s0.y, msum);
-                msum = fmaf((float)((m_lo >> 16) & 0xFFu), s0.z, msum);
-                msum = fmaf((float)(m_lo >> 24), s0.w, msum);
-                msum = fmaf((float)(m_hi & 0xFFu), s1.x, msum);
-                msum = fmaf((float)((m_hi >> 8) & 0xFFu), s1.y, msum);
-                msum = fmaf((float)((m_hi >> 16) & 0xFFu), s1.z, msum);
-                msum = fmaf((float)(m_hi >> 24), s1.w, msum);
-#pragma unroll
-                for (int s = 0; s < NS; ++s)
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        if (s * R + r == sr) mins[s][r] = fmaf(dmin, msum, mins[s][r]);
-                const uint32_t te = table + (uint32_t)((sr * cs + sbl) * 64);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(te + (uint32_t)cc * 16u),
-                                 "f"(dsc[2 * cc]), "f"(dsc[2 * cc]), "f"(dsc[2 * cc + 1]), "f"(dsc[2 * cc + 1])
-                                 : "memory");
+                sbl += 32;
+                while (sbl >= cs) {
+                    sbl -= cs;
+                    ++sr;
+                }
             }
         }
         __syncwarp();
@@ -239,37 +281,37 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 w = lds128(slot + (uint32_t)(((s * R + r) * cs + sbl) * 144 + 16) + cpos * 16u);
-                        fold[s][r] ^= w.x ^ w.y ^ w.z ^ w.w;
+                    for (int rr = 0; rr < R; ++rr) {
+                        const uint4 w = lds128(slot + (uint32_t)(((s * R + rr) * cs + sbl) * 144 + 16) + cpos * 16u);
+                        fold[s][rr] ^= w.x ^ w.y ^ w.z ^ w.w;
                     }
             } else {
+                const uint32_t xa = xs + u * 16u;
+                const uint32_t qstride = U * 16u;
                 float4 xl[4], xh[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    xl[i] = lds128f(xs + xs_index(0u, (uint32_t)i, u, U) * 4u);
-                    xh[i] = lds128f(xs + xs_index(0u, (uint32_t)(4 + i), u, U) * 4u);
+                    xl[i] = lds128f(xa + (uint32_t)i * qstride);
+                    xh[i] = lds128f(xa + (uint32_t)(4 + i) * qstride);
                 }
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t blk = (uint32_t)(((s * R + r) * cs + sbl) * 144);
-                        const uint4 w = lds128(slot + blk + 16u + cpos * 16u);
+                    for (int rr = 0; rr < R; ++rr) {
+                        const int it = (s * R + rr) * cs + sbl;
+                        const uint4 w = lds128(slot + (uint32_t)(it * 144 + 16) + cpos * 16u);
                         float2 aL = make_float2(0.f, 0.f), aH = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const uint32_t word = i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
-                            const Word8 d8 = decode_word<0>(word);
+                            const Word8s d8 = decode_word_sub(i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w);
                             aL = ffma2(d8.lo01, make_float2(xl[i].x, xl[i].y), aL);
                             aL = ffma2(d8.lo23, make_float2(xl[i].z, xl[i].w), aL);
                             aH = ffma2(d8.hi01, make_float2(xh[i].x, xh[i].y), aH);
                             aH = ffma2(d8.hi23, make_float2(xh[i].z, xh[i].w), aH);
                         }
-                        const float4 tb =
-                            lds128f(table + (uint32_t)(((s * R + r) * cs + sbl) * 64) + (cpos >> 1) * 16u);
-                        tot[s][r] = ffma2(make_float2(tb.x, tb.y), aL, tot[s][r]);
-                        tot[s][r] = ffma2(make_float2(tb.z, tb.w), aH, tot[s][r]);
+                        const float4 tb = lds128f(table + (uint32_t)(it * 64) + (cpos >> 1) * 16u);
+                        tot[s][rr] = ffma2(make_float2(tb.x, tb.y), aL, tot[s][rr]);
+                        tot[s][rr] = ffma2(make_float2(tb.z, tb.w), aH, tot[s][rr]);
                     }
             }
         }
@@ -281,12 +323,12 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
+                    for (int rr = 0; rr < R; ++rr) {
 #pragma unroll
                         for (int off = 16; off >= 1; off >>= 1)
-                            fold[s][r] ^= __shfl_xor_sync(0xffffffffu, fold[s][r], off);
-                        if (lane == 0 && r < rv) (s == 0 ? p.y0 : p.y1)[r0 + r] = __uint_as_float(fold[s][r]);
-                        fold[s][r] = 0u;
+                            fold[s][rr] ^= __shfl_xor_sync(0xffffffffu, fold[s][rr], off);
+                        if (lane == 0 && rr < rv) (s == 0 ? p.y0 : p.y1)[r0 + rr] = __uint_as_float(fold[s][rr]);
+                        fold[s][rr] = 0u;
                     }
             } else {
                 constexpr int NV = NS * R;
@@ -298,21 +340,26 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        vals[s * R + r] = (tot[s][r].x + tot[s][r].y) - mins[s][r];
-                        tot[s][r] = make_float2(0.f, 0.f);
-                        mins[s][r] = 0.f;
+                    for (int rr = 0; rr < R; ++rr) {
+                        vals[s * R + rr] = (tot[s][rr].x + tot[s][rr].y) - mins[s][rr];
+                        tot[s][rr] = make_float2(0.f, 0.f);
+                        mins[s][rr] = 0.f;
                     }
                 warp_transpose_reduce<P2>(vals, lane);
                 const int idx = lane >> (5 - L2);
                 const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
                 if (leader && idx < NV) {
                     const int s = idx / R;
-                    const int r = idx - s * R;
-                    if (r < rv) (s == 0 ? p.y0 : p.y1)[r0 + r] = vals[0];
+                    const int rr = idx - s * R;
+                    if (rr < rv) (s == 0 ? p.y0 : p.y1)[r0 + rr] = vals[0];
                 }
             }
         }
+        if (++c == p.S) {
+            c = 0;
+            job += Wtot;
+        }
+        cslot = cslot + 1 == D ? 0 : cslot + 1;
     }
 }
 
@@ -364,15 +411,19 @@ __global__ void q4k_dequant_kernel(float* __restrict__ W, const uint8_t* __restr
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-void plan_override(int* cs, int* d) {
-    static int o_cs = -1, o_d = -1;
+// Developer override of the launch plan, read once from Q4GEMV_Q4K_PLAN="CS,depth,variant" (super-blocks
+// per chunk, ring depth; variant 2: gate+up as 2 rows x 8 warps instead of 1 row x 16 warps). Used for
+// tuning sweeps; the defaults come from such sweeps.
+void plan_override(int* cs, int* d, int* variant) {
+    static int o_cs = -1, o_d = -1, o_v = -1;
     static std::once_flag once;
     std::call_once(once, [] {
         const char* e = getenv("Q4GEMV_Q4K_PLAN");
-        if (e) sscanf(e, "%d,%d", &o_cs, &o_d);
+        if (e) sscanf(e, "%d,%d,%d", &o_cs, &o_d, &o_v);
     });
     if (o_cs > 0) *cs = o_cs;
     if (o_d > 0) *d = o_d;
+    if (o_v > 0) *variant = o_v;
 }
 
 struct Args {
@@ -396,12 +447,12 @@ cudaError_t launch_plan(const DeviceInfo& di, Q4KParams p, uint32_t smem, cudaSt
     return launch_kernel(kern, grid, W * 32, smem, s, p);
 }
 
-// Shared memory: [staged xhat K*4][sub-block sums K/32*4][W reduction floats][W header tables]
-//                [W rings of D slots]. Chunk (super-blocks per slot) and depth shrink until it fits.
+// Shared memory: [staged xhat K*4][(S_j, 2^(22+e_j)) per sub-block K/32*8][W reduction floats]
+//                [W header tables][W rings of D slots]. Chunk (super-blocks per slot) and depth shrink until
+//                it fits.
 template <int NS, int R, int W, bool PURE>
 cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t s) {
     const int nsb = a.K / 256;
-    plan_override(&CS, &D);
     D = std::max(2, std::min(4, D));
     Q4KParams p;
     bool ok = false;
@@ -413,7 +464,7 @@ cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t
             const int slot = round_up(NS * R * cs * 144, 128);
             const int tbytes = round_up(NS * R * cs * 64, 128);
             const uint32_t xs_bytes = PURE ? 0u : (uint32_t)(a.K * 4);
-            const uint32_t ss_bytes = PURE ? 0u : (uint32_t)round_up(a.K / 32 * 4, 128);
+            const uint32_t ss_bytes = PURE ? 0u : (uint32_t)round_up(a.K / 32 * 8, 128);
             const uint32_t red_bytes = (uint32_t)round_up(W * 4, 128);
             p.xs_off = 0;
             p.ssum_off = xs_bytes;
@@ -458,8 +509,14 @@ cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
     const Args a{y0, y1, w0, w1, x, gamma, eps, N, K};
-    if (w1) return run<2, 1, 16, false>(di, a, 14, 2, s);
-    return run<1, 2, 16, false>(di, a, 14, 2, s);
+    int cs = 16, depth = 2, variant = 1;
+    plan_override(&cs, &depth, &variant);
+    if (w1) {
+        if (variant == 2) return run<2, 2, 8, false>(di, a, cs, depth, s);
+        return run<2, 1, 16, false>(di, a, cs, depth, s);
+    }
+    if (variant == 2) return run<1, 4, 8, false>(di, a, cs, depth, s);
+    return run<1, 2, 16, false>(di, a, cs, depth, s);
 }
 
 cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s) {
@@ -467,7 +524,9 @@ cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cu
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
     const Args a{sink, nullptr, w, nullptr, nullptr, nullptr, 0.f, N, K};
-    return run<1, 2, 16, true>(di, a, 14, 2, s);
+    int cs = 16, depth = 2, variant = 1;
+    plan_override(&cs, &depth, &variant);
+    return run<1, 2, 16, true>(di, a, cs, depth, s);
 }
 
 cudaError_t launch_q4k_dequant(float* W, const uint8_t* w, int N, int K, cudaStream_t s) {

@@ -120,43 +120,42 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     grid_launch_dependents();
 
     if constexpr (!PURE) {
-        // Stage the V vectors (X is [V][K]): each thread takes whole 32-element blocks, issues the eight
-        // float4 loads of kStageB blocks before using any, sums each block and finds its largest magnitude
-        // in registers, and stores it pre-scaled with its own exponent bound. Consecutive threads hold
-        // consecutive blocks, so each quad store of a warp covers 512 consecutive bytes.
+        // Stage the V vectors (X is [V][K]): four lanes per 32-element block, lane t of the group holding
+        // float4 2t and 2t+1 (quads 2t, 2t+1 of the unit); loads are issued kStageU/2 blocks ahead. The loop
+        // covers whole warps (the block count rounded up to 8) so the group shuffles always see 32 lanes.
         const int nb_all = V * p.nblk;
-        for (int base = threadIdx.x; base < nb_all; base += kThreads * kStageB) {
-            float4 xv[kStageB][8];
+        const int t4 = lane & 3;
+        const int nthr = ((nb_all * 4 + 31) & ~31);
+        for (int base = threadIdx.x; base < nthr; base += kThreads * (kStageU / 2)) {
+            float4 xa[kStageU / 2], xb[kStageU / 2];
 #pragma unroll
-            for (int j = 0; j < kStageB; ++j) {
-                const int blk = base + j * kThreads;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    xv[j][q] = blk < nb_all ? __ldg(reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + q)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < kStageU / 2; ++j) {
+                const int blk = (base + j * kThreads) >> 2;
+                const bool in = blk < nb_all;
+                const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * t4;
+                xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int j = 0; j < kStageB; ++j) {
-                const int blk = base + j * kThreads;
+            for (int j = 0; j < kStageU / 2; ++j) {
+                const int thr = base + j * kThreads;
+                if (thr >= nthr) break;  // warp-uniform
+                const int blk = thr >> 2;
+                const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
                 if (blk < nb_all) {
                     const int v = blk / p.nblk;
                     const uint32_t u = (uint32_t)(blk - v * p.nblk);
-                    float bsum, bmax;
-                    block_sum_max(xv[j], bsum, bmax);
-                    const int e = block_exponent(bmax);
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        // float4 q8 of the block holds elements 4*q8 .. 4*q8+3: half q8/4, word q8%4
-                        const int hi = q8 >> 2;
-                        const uint32_t a = xs + xs_chunk_offset((uint32_t)v, (uint32_t)q8, u, (uint32_t)V);
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                     "f"(stage_scaled(xv[j][q8].x, hi, 0, e)), "f"(stage_scaled(xv[j][q8].y, hi, 1, e)),
-                                     "f"(stage_scaled(xv[j][q8].z, hi, 2, e)), "f"(stage_scaled(xv[j][q8].w, hi, 3, e))
-                                     : "memory");
-                    }
-                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset((uint32_t)v, u, (uint32_t)V)),
-                                 "f"(block_factor(e)), "f"(-8.0f * bsum)
+                    const uint32_t a0 = xs + xs_chunk_offset((uint32_t)v, (uint32_t)(2 * t4), u, (uint32_t)V);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
+                                 "f"(st.a.z), "f"(st.a.w)
                                  : "memory");
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 512u), "f"(st.b.x), "f"(st.b.y),
+                                 "f"(st.b.z), "f"(st.b.w)
+                                 : "memory");
+                    if (t4 == 0)
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset((uint32_t)v, u, (uint32_t)V)),
+                                     "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
+                                     : "memory");
                 }
             }
         }

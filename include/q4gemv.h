@@ -38,7 +38,10 @@
  *
  * Numerics: products and sums run in fp32 (packed fp32x2 FMAs), so results differ from exact arithmetic by
  * the order of summation; the library's tests hold every output within 1e-3 * sum_k |w_k||x_k| + 1e-5 of
- * an fp64 reference. The dequant entry points are bit-exact.
+ * an fp64 reference. The dequant entry points are bit-exact. Supported input range: the kernels stage each
+ * 32-element block of x (or of the normalised x for Q4_K) scaled by a power of two chosen from its largest
+ * magnitude; planar Q4 blocks must stay below 2^105 in magnitude and Q4_K blocks below 2^83, beyond which the
+ * affected outputs are non-finite. Small inputs keep their relative accuracy down to the fp32 subnormal range.
  */
 #ifndef Q4GEMV_H
 #define Q4GEMV_H
@@ -69,8 +72,9 @@ enum {
  * Source: inferencelayer kernel_lab.rs, shader GEMV_F16S (one column of its output).
  *   y   float[N]          output                       (4-byte aligned)
  *   qs  uint8[N][K/32][16] packed codes                (16-byte aligned)
- *   d   uint16[N][K/32]   binary16 block scales        (2-byte aligned; 16-byte aligned and K % 256 == 0
- *                                                       let the scales ride the bulk copies)
+ *   d   uint16[N][K/32]   binary16 block scales        (2-byte aligned; when 16-byte aligned and K % 256 == 0
+ *                                                       the scales travel in the same 16-byte async copies
+ *                                                       as the codes, otherwise each is read directly)
  *   x   float[K]          input                        (16-byte aligned)
  *   N >= 1; K >= 32 and K % 32 == 0.
  */

@@ -40,6 +40,7 @@ cudaError_t gemv_v1(const DeviceInfo& di, float* Y, const uint8_t* qs, const uin
         case 14: e = launch<1, 2, 14, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
         case 13: e = launch<1, 2, 12, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
         case 10: e = launch<1, 2, 10, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
+        case 24: e = launch<1, 1, 24, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
         case 8:
             if (K / 32 <= 128) e = launch<1, 4, 8, 2, true, false>(di, Y, qs, d, X, N, K, 2, 4, s);
             break;

@@ -13,12 +13,11 @@
 //    bound e_j (the bias-free decode of device_common.cuh), next to (S_j = sum of xhat over j, 2^(22+e_j));
 //  * each warp streams R rows of each of NS weight matrices (whole rows when they fit) through its own ring
 //    of cp.async slots, with incremental per-stage control;
-//  * per slot, the warp first decodes each super-block header once: d*sc_j*2^(22+e_j) into a small table
-//    (so the unit loop needs no per-block factor), and the whole min term dmin * sum_j m_j * S_j straight
-//    into its row accumulators;
-//  * then lane l takes 16-byte quant unit l (+32, ...): chunk c = (l%8)/2, half h = l%2 of a super-block,
-//    i.e. 16 codes of sub-block 2c and 16 of 2c+1 against the same 32 staged inputs: one shift and eight
-//    ANDs per word, packed fp32x2 FMAs into one accumulator per sub-block, folded with the table entries;
+//  * lane l takes 16-byte quant unit l (+32, ...): chunk c = (l%8)/2, half h = l%2 of a super-block, i.e.
+//    16 codes of sub-block 2c and 16 of 2c+1 against the same 32 staged inputs: one shift and eight ANDs per
+//    word, packed fp32x2 FMAs into one accumulator per sub-block. The 8 lanes of a super-block each decode
+//    one sub-block's header entry (j = l%8): d*sc_j*2^(22+e_j), shared with the group by two shuffles, and
+//    the min term dmin*m_j*S_j, added to the lane's own accumulator (the warp reduction sums them);
 //  * row totals are summed over the warp and stored. The NS matrices share every staged-input load.
 // Inputs whose staged value reaches 2^83 in magnitude are outside the supported range (non-finite result).
 #include <algorithm>
@@ -46,8 +45,7 @@ struct Q4KParams {
     int S;            // chunks per row
     int jobs;         // row groups of R rows (per stream)
     int slot_bytes;   // multiple of 128
-    int table_bytes;  // per warp
-    uint32_t xs_off, ssum_off, red_off, tables_off, slots_off;
+    uint32_t xs_off, ssum_off, red_off, slots_off;
 };
 
 // byte j of w as an exact float (0x4B000000 | b is 2^23 + b)
@@ -67,7 +65,6 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
     const uint32_t xs = s_base + p.xs_off;
     const uint32_t ssum = s_base + p.ssum_off;
     const uint32_t red = s_base + p.red_off;
-    const uint32_t table = s_base + p.tables_off + (uint32_t)(warp * p.table_bytes);
     const uint32_t ring = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
 
     // Warps are numbered across CTAs first so that a small job count still spreads over all SMs.
@@ -206,86 +203,37 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
         const int rv = min(R, p.N - r0);
         const int sb0 = c * p.CS;
         const int cs = min(p.CS, p.nsb - sb0);
-        const int nitems = NS * R * cs;
 
-        // 1) headers: one lane per (stream, row, super-block) item; sr = item / cs, kept incrementally
-        {
-            int sr = 0, sbl = lane;
-            while (sbl >= cs && sr < NS * R) {
-                sbl -= cs;
-                ++sr;
-            }
-            for (int t = lane; t < nitems; t += 32) {
-                const uint4 hdr = lds128(slot + (uint32_t)(t * 144));
-                if constexpr (PURE) {
-#pragma unroll
-                    for (int s = 0; s < NS; ++s)
-#pragma unroll
-                        for (int rr = 0; rr < R; ++rr)
-                            if (s * R + rr == sr) fold[s][rr] ^= hdr.x ^ hdr.y ^ hdr.z ^ hdr.w;
-                } else {
-                    const float d = f16_bits_to_f32(hdr.x);
-                    const float dmin = f16_bits_to_f32(hdr.x >> 16);
-                    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu;
-                    const uint32_t m_lo = hdr.z & 0x3F3F3F3Fu;
-                    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-                    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-                    const uint32_t sg = (uint32_t)(sb0 + sbl) * 8u;  // first sub-block index in the row
-                    float f[8], sm[8];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 pr = lds128f(ssum + (sg + 2u * (uint32_t)q) * 8u);  // (S, 2^(22+e)) x 2
-                        sm[2 * q] = pr.x;
-                        f[2 * q] = pr.y;
-                        sm[2 * q + 1] = pr.z;
-                        f[2 * q + 1] = pr.w;
-                    }
-                    float msum = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        msum = fmaf(byte_as_float(m_lo, j), sm[j], msum);
-                        msum = fmaf(byte_as_float(m_hi, j), sm[j + 4], msum);
-                    }
-#pragma unroll
-                    for (int s = 0; s < NS; ++s)
-#pragma unroll
-                        for (int rr = 0; rr < R; ++rr)
-                            if (s * R + rr == sr) mins[s][rr] = fmaf(dmin, msum, mins[s][rr]);
-                    float dsc[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        dsc[j] = (d * byte_as_float(sc_lo, j)) * f[j];
-                        dsc[j + 4] = (d * byte_as_float(sc_hi, j)) * f[j + 4];
-                    }
-                    const uint32_t te = table + (uint32_t)(t * 64);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(te + (uint32_t)cc * 16u),
-                                     "f"(dsc[2 * cc]), "f"(dsc[2 * cc]), "f"(dsc[2 * cc + 1]), "f"(dsc[2 * cc + 1])
-                                     : "memory");
-                }
-                sbl += 32;
-                while (sbl >= cs) {
-                    sbl -= cs;
-                    ++sr;
-                }
-            }
-        }
-        __syncwarp();
-
-        // 2) quant units
-        for (int ul = lane; ul < 8 * cs; ul += 32) {
-            const int sbl = ul >> 3;
+        // Quant units: lane l takes unit l (+32, ...) of the chunk, i.e. super-block ul/8 at position
+        // cpos = ul%8 (chunk cpos/2, half cpos%2). The trip count is uniform over the warp (lanes past the
+        // chunk work on a clamped super-block and add nothing), so every lane takes part in the shuffles.
+        // Each lane decodes the header entry of sub-block j = cpos of its super-block: d*sc_j*2^(22+e_j)
+        // (exchanged within the 8-lane group: a unit needs sub-blocks 2c and 2c+1) and its own min term
+        // dmin*m_j*S_j, which it adds to its row accumulator; the warp reduction sums all eight.
+        const int nunits = 8 * cs;
+        const int gbase = lane & ~7;
+#pragma unroll 1
+        for (int ul0 = 0; ul0 < nunits; ul0 += 32) {
+            const int ul = ul0 + lane;
+            const bool valid = ul < nunits;
+            const int sbl = valid ? (ul >> 3) : 0;
             const uint32_t u = (uint32_t)(8 * (sb0 + sbl)) + cpos;
             if constexpr (PURE) {
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) {
-                        const uint4 w = lds128(slot + (uint32_t)(((s * R + rr) * cs + sbl) * 144 + 16) + cpos * 16u);
-                        fold[s][rr] ^= w.x ^ w.y ^ w.z ^ w.w;
+                        const int it = (s * R + rr) * cs + sbl;
+                        const uint4 w = lds128(slot + (uint32_t)(it * 144 + 16) + cpos * 16u);
+                        uint32_t f = w.x ^ w.y ^ w.z ^ w.w;
+                        if (cpos == 0) {
+                            const uint4 hdr = lds128(slot + (uint32_t)(it * 144));
+                            f ^= hdr.x ^ hdr.y ^ hdr.z ^ hdr.w;
+                        }
+                        if (valid) fold[s][rr] ^= f;
                     }
             } else {
+                const float2 sf = lds64f(ssum + u * 8u);  // (S_j, 2^(22+e_j)) of sub-block j = cpos of this super-block
                 const uint32_t xa = xs + u * 16u;
                 const uint32_t qstride = U * 16u;
                 float4 xl[4], xh[4];
@@ -294,11 +242,24 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
                     xl[i] = lds128f(xa + (uint32_t)i * qstride);
                     xh[i] = lds128f(xa + (uint32_t)(4 + i) * qstride);
                 }
+                const uint32_t jj = cpos & 3u;
 #pragma unroll
                 for (int s = 0; s < NS; ++s)
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) {
                         const int it = (s * R + rr) * cs + sbl;
+                        const uint4 hdr = lds128(slot + (uint32_t)(it * 144));
+                        // 6-bit scale and min of sub-block j = cpos
+                        const uint32_t scw = cpos < 4 ? (hdr.y & 0x3F3F3F3Fu)
+                                                      : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+                        const uint32_t mw = cpos < 4 ? (hdr.z & 0x3F3F3F3Fu)
+                                                     : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+                        const float d = f16_bits_to_f32(hdr.x);
+                        const float dmin = f16_bits_to_f32(hdr.x >> 16);
+                        const float dsc = (d * byte_as_float(scw, (int)jj)) * sf.y;
+                        const float mterm = (dmin * byte_as_float(mw, (int)jj)) * sf.x;
+                        const float dlo = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos & ~1u));
+                        const float dhi = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos | 1u));
                         const uint4 w = lds128(slot + (uint32_t)(it * 144 + 16) + cpos * 16u);
                         float2 aL = make_float2(0.f, 0.f), aH = make_float2(0.f, 0.f);
 #pragma unroll
@@ -309,14 +270,16 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
                             aH = ffma2(d8.hi01, make_float2(xh[i].x, xh[i].y), aH);
                             aH = ffma2(d8.hi23, make_float2(xh[i].z, xh[i].w), aH);
                         }
-                        const float4 tb = lds128f(table + (uint32_t)(it * 64) + (cpos >> 1) * 16u);
-                        tot[s][rr] = ffma2(make_float2(tb.x, tb.y), aL, tot[s][rr]);
-                        tot[s][rr] = ffma2(make_float2(tb.z, tb.w), aH, tot[s][rr]);
+                        if (valid) {
+                            tot[s][rr] = ffma2(make_float2(dlo, dlo), aL, tot[s][rr]);
+                            tot[s][rr] = ffma2(make_float2(dhi, dhi), aH, tot[s][rr]);
+                            mins[s][rr] += mterm;
+                        }
                     }
             }
         }
 
-        __syncwarp();  // every lane is done with this slot (and its table) before later stages reuse them
+        __syncwarp();  // every lane is done with this slot before a later stage reuses it
 
         if (c == p.S - 1) {
             if constexpr (PURE) {
@@ -448,8 +411,7 @@ cudaError_t launch_plan(const DeviceInfo& di, Q4KParams p, uint32_t smem, cudaSt
 }
 
 // Shared memory: [staged xhat K*4][(S_j, 2^(22+e_j)) per sub-block K/32*8][W reduction floats]
-//                [W header tables][W rings of D slots]. Chunk (super-blocks per slot) and depth shrink until
-//                it fits.
+//                [W rings of D slots]. Chunk (super-blocks per slot) and depth shrink until it fits.
 template <int NS, int R, int W, bool PURE>
 cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t s) {
     const int nsb = a.K / 256;
@@ -462,21 +424,18 @@ cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t
         for (int cs0 = CS; cs0 >= 1 && !ok; cs0 /= 2) {
             const int cs = std::min(cs0, nsb);
             const int slot = round_up(NS * R * cs * 144, 128);
-            const int tbytes = round_up(NS * R * cs * 64, 128);
             const uint32_t xs_bytes = PURE ? 0u : (uint32_t)(a.K * 4);
             const uint32_t ss_bytes = PURE ? 0u : (uint32_t)round_up(a.K / 32 * 8, 128);
             const uint32_t red_bytes = (uint32_t)round_up(W * 4, 128);
             p.xs_off = 0;
             p.ssum_off = xs_bytes;
             p.red_off = p.ssum_off + ss_bytes;
-            p.tables_off = p.red_off + red_bytes;
-            p.slots_off = p.tables_off + (uint32_t)(W * tbytes);
+            p.slots_off = p.red_off + red_bytes;
             smem = p.slots_off + (uint32_t)(W * dd * slot);
             if (smem <= (uint32_t)di.max_smem_optin) {
                 ok = true;
                 p.CS = cs;
                 p.slot_bytes = slot;
-                p.table_bytes = tbytes;
                 depth = dd;
             }
         }
@@ -513,6 +472,7 @@ cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8
     plan_override(&cs, &depth, &variant);
     if (w1) {
         if (variant == 2) return run<2, 2, 8, false>(di, a, cs, depth, s);
+        if (variant == 3) return run<2, 1, 24, false>(di, a, cs, depth, s);
         return run<2, 1, 16, false>(di, a, cs, depth, s);
     }
     if (variant == 2) return run<1, 4, 8, false>(di, a, cs, depth, s);

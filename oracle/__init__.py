@@ -57,6 +57,12 @@ class Oracle:
                                                    _f64p, _f64p, _f64p, _f64p]
         L.oracle_moe_q4_gemv.argtypes = [_u8p, _u16p, _u8p, _u16p, _f32p, _i32p, _i64, _i64, _i64, _i64,
                                          _i64, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_silu.restype = ctypes.c_double
+        L.oracle_silu.argtypes = [ctypes.c_double]
+        L.oracle_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
+        L.oracle_topk_softmax_f32.argtypes = [_f32p, _i64, _i64, _i64, ctypes.c_int, _i32p, _f64p]
+        L.oracle_moe_router.argtypes = [_u8p, _u16p, _f32p, _i64, _i64, _i64, _i64, ctypes.c_int, _f64p, _f64p,
+                                        _i32p, _f64p]
         self.L = L
 
     # -- element decode ------------------------------------------------------------------------
@@ -173,6 +179,45 @@ class Oracle:
                                        _p(bg, _f64p), _p(bu, _f64p))
         assert rc == 0
         return (yg, bg), (yu, bu)
+
+
+    # -- epilogue and router ---------------------------------------------------------------------
+    def silu(self, g: float) -> float:
+        return float(self.L.oracle_silu(float(g)))
+
+    def swiglu(self, g, u) -> np.ndarray:
+        g = _c(g, np.float64)
+        u = _c(u, np.float64)
+        assert g.shape == u.shape
+        y = np.empty(g.shape, np.float64)
+        self.L.oracle_swiglu(_p(g, _f64p), _p(u, _f64p), g.size, _p(y, _f64p))
+        return y
+
+    def topk_softmax_f32(self, logits, topk: int, normalize: bool):
+        lg = _c(np.atleast_2d(logits), np.float32)
+        T, E = lg.shape
+        ids = np.empty((T, topk), np.int32)
+        w = np.empty((T, topk), np.float64)
+        self.L.oracle_topk_softmax_f32(_p(lg, _f32p), T, E, topk, 1 if normalize else 0, _p(ids, _i32p), _p(w, _f64p))
+        return ids, w
+
+    def moe_router(self, qs, d, x, topk: int, normalize: bool):
+        """(logits [T][E], bounds [T][E], ids [T][topk], weights [T][topk]) for planar-Q4 router rows."""
+        qs = _c(qs, np.uint8)
+        d = _c(np.asarray(d, dtype=np.float16).view(np.uint16), np.uint16)
+        x = _c(np.atleast_2d(x), np.float32)
+        E, nblk = d.shape
+        K = nblk * 32
+        T = x.shape[0]
+        assert x.shape == (T, K)
+        lg = np.empty((T, E), np.float64)
+        bd = np.empty((T, E), np.float64)
+        ids = np.empty((T, topk), np.int32)
+        w = np.empty((T, topk), np.float64)
+        rc = self.L.oracle_moe_router(_p(qs, _u8p), _p(d, _u16p), _p(x, _f32p), T, E, K, topk, 1 if normalize else 0,
+                                      _p(lg, _f64p), _p(bd, _f64p), _p(ids, _i32p), _p(w, _f64p))
+        assert rc == 0
+        return lg, bd, ids, w
 
 
 _default: Oracle | None = None

@@ -26,6 +26,13 @@
  *     rows e*N .. e*N+N-1 of one stacked store; slot (t, s) uses expert ids[t*topk+s] on token t and
  *     writes output (t*topk+s)*N + r.
  *
+ *   - MoE router: spark_model `gemm_quant.rs`, moe_gate_topk_fused: gate[e] = x . Wgate[e] for every
+ *     expert (here Wgate is planar Q4, one row per expert), then the top-K experts and their softmax
+ *     weights. Reading: softmax over all E logits (max subtracted), the K largest logits in descending
+ *     order with ties to the lower expert index, and with `normalize` the K weights divided by their sum.
+ *   - SwiGLU: silu(g) * u with silu(g) = g / (1 + exp(-g)) (the standard gated-linear-unit epilogue; the
+ *     pages only show that production MoE keeps one value per routed row).
+ *
  * Every GEMV entry also returns bound[i] = sum_k |W[n][k]| * |xhat[k]|, the scale of the tolerance
  * the comparisons use.
  *
@@ -243,5 +250,74 @@ int oracle_moe_q4_gemv(const uint8_t *qs_gate, const uint16_t *d_gate, const uin
         }
     }
     free(w);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Epilogue and router                                                                          */
+/* ------------------------------------------------------------------------------------------ */
+
+double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* y[i] = silu(g[i]) * u[i] in fp64. */
+void oracle_swiglu(const double *g, const double *u, int64_t n, double *y)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_silu(g[i]) * u[i];
+}
+
+/*
+ * Top-K softmax of one row of E logits (given as float or double through `get`): ids[0..topk) are the
+ * indices of the topk largest logits in descending order (ties: lower index first); weights[i] is the
+ * softmax probability of ids[i] over all E logits, divided by the sum of the topk probabilities when
+ * `normalize` is non-zero. Plain selection: topk passes over the logits.
+ */
+static void topk_softmax_row(const double *lg, int64_t E, int64_t topk, int normalize, int32_t *ids, double *weights)
+{
+    double mx = -INFINITY;
+    for (int64_t e = 0; e < E; ++e)
+        if (lg[e] > mx) mx = lg[e];
+    double z = 0.0;
+    for (int64_t e = 0; e < E; ++e) z += exp(lg[e] - mx);
+    for (int64_t i = 0; i < topk; ++i) {
+        int64_t best = -1;
+        for (int64_t e = 0; e < E; ++e) {
+            int taken = 0;
+            for (int64_t j = 0; j < i; ++j)
+                if (ids[j] == e) taken = 1;
+            if (taken) continue;
+            if (best < 0 || lg[e] > lg[best]) best = e;
+        }
+        ids[i] = (int32_t)best;
+        weights[i] = exp(lg[best] - mx) / z;
+    }
+    if (normalize) {
+        double s = 0.0;
+        for (int64_t i = 0; i < topk; ++i) s += weights[i];
+        for (int64_t i = 0; i < topk; ++i) weights[i] /= s;
+    }
+}
+
+/* Top-K softmax over T rows of fp32 logits [T][E] (the selection made on exactly these values). */
+void oracle_topk_softmax_f32(const float *logits, int64_t T, int64_t E, int64_t topk, int normalize,
+                             int32_t *ids, double *weights)
+{
+    double *row = (double *)malloc((size_t)E * sizeof(double));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) row[e] = (double)logits[t * E + e];
+        topk_softmax_row(row, E, topk, normalize, ids + t * topk, weights + t * topk);
+    }
+    free(row);
+}
+
+/*
+ * MoE router: logits[t][e] = sum_k Wgate[e][k] * x[t][k] (planar Q4, E rows of K), with bounds, then
+ * top-K softmax of each token's fp64 logits.
+ */
+int oracle_moe_router(const uint8_t *qs, const uint16_t *d, const float *x, int64_t T, int64_t E, int64_t K,
+                      int64_t topk, int normalize, double *logits, double *bound, int32_t *ids, double *weights)
+{
+    int rc = oracle_q4_gemv_batched(qs, d, x, T, E, K, logits, bound);
+    if (rc) return rc;
+    for (int64_t t = 0; t < T; ++t) topk_softmax_row(logits + t * E, E, topk, normalize, ids + t * topk, weights + t * topk);
     return 0;
 }

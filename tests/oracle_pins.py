@@ -329,6 +329,82 @@ def pin_moe(o):
     assert np.array_equal(yg3[keep], yg[keep])
 
 
+def pin_silu(o):
+    """silu against the logistic function of a library (scipy.special.expit), its odd-part identity
+    silu(x) - silu(-x) = x, its value and slope at 0 and its limits."""
+    from scipy.special import expit
+
+    assert o.silu(0.0) == 0.0
+    xs = np.concatenate([np.linspace(-30, 30, 241), [1e-8, -1e-8, 0.5, -0.5, 7.25]])
+    for x in xs:
+        v = o.silu(x)
+        assert abs(v - x * float(expit(x))) <= 1e-15 * max(1.0, abs(x)), x
+        assert abs((v - o.silu(-x)) - x) <= 4e-16 * max(1.0, abs(x)), x
+    h = 1e-6
+    assert abs((o.silu(h) - o.silu(-h)) / (2 * h) - 0.5) < 1e-9  # slope 1/2 at 0
+    assert o.silu(80.0) == 80.0 and -1e-30 < o.silu(-80.0) < 0.0
+
+
+def pin_swiglu(o):
+    """swiglu(g, u) is silu(g) in the first argument and linear in the second."""
+    rng = np.random.default_rng(30)
+    g = rng.standard_normal(64) * 4
+    u = rng.standard_normal(64)
+    y = o.swiglu(g, u)
+    assert np.array_equal(o.swiglu(g, np.ones(64)), np.array([o.silu(v) for v in g]))
+    assert np.array_equal(o.swiglu(g, 2 * u), 2 * y)
+    assert np.array_equal(o.swiglu(g, np.zeros(64)), np.zeros(64))
+    assert np.array_equal(o.swiglu(np.zeros(64), u), np.zeros(64))
+
+
+def pin_topk_softmax(o):
+    """Top-K softmax: a hand-worked example with a tie, then random rows against a stable argsort and the
+    softmax of a library (scipy.special.softmax), with and without renormalisation."""
+    from scipy.special import softmax
+
+    lg = np.array([[0.5, 2.0, -1.0, 2.0, 1.5]], np.float32)
+    ids, w = o.topk_softmax_f32(lg, 3, False)
+    assert ids.tolist() == [[1, 3, 4]]  # 2.0 (index 1, then index 3), then 1.5
+    p = np.exp(lg[0].astype(np.float64) - 2.0)
+    p /= p.sum()
+    assert np.allclose(w[0], p[[1, 3, 4]], rtol=1e-15, atol=0)
+    ids2, w2 = o.topk_softmax_f32(lg, 3, True)
+    assert ids2.tolist() == [[1, 3, 4]] and np.allclose(w2[0], p[[1, 3, 4]] / p[[1, 3, 4]].sum(), rtol=1e-15)
+    rng = np.random.default_rng(31)
+    for E, K in ((64, 8), (16, 2), (7, 7), (128, 1)):
+        L = (rng.standard_normal((5, E)) * 3).astype(np.float32)
+        L[0, 3] = L[0, 5]  # a tie
+        for norm in (False, True):
+            ids, w = o.topk_softmax_f32(L, K, norm)
+            for t in range(5):
+                order = np.argsort(-L[t].astype(np.float64), kind="stable")[:K]
+                assert ids[t].tolist() == order.tolist()
+                pt = softmax(L[t].astype(np.float64))[order]
+                if norm:
+                    pt = pt / pt.sum()
+                assert np.allclose(w[t], pt, rtol=1e-13, atol=0)
+
+
+def pin_router(o):
+    """Router logits are the dense product of the decoded router rows; ids and weights are the top-K
+    softmax of those logits (stable argsort, library softmax)."""
+    from scipy.special import softmax
+
+    rng = np.random.default_rng(32)
+    E, K, T, topk = 16, 256, 3, 4
+    qs, d = synth.q4_weights(rng, E, K)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    W = o.dequant_q4(qs, d).astype(np.float64)
+    lg, bd, ids, w = o.moe_router(qs, d, x, topk, True)
+    assert np.allclose(lg, x.astype(np.float64) @ W.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bd, np.abs(x.astype(np.float64)) @ np.abs(W).T, rtol=1e-12)
+    for t in range(T):
+        order = np.argsort(-lg[t], kind="stable")[:topk]
+        assert ids[t].tolist() == order.tolist()
+        pt = softmax(lg[t])[order]
+        assert np.allclose(w[t], pt / pt.sum(), rtol=1e-13)
+
+
 ALL_PINS = [
     pin_f16_decode,
     pin_q4_nibble_positions,
@@ -344,4 +420,8 @@ ALL_PINS = [
     pin_q4k_gemv_matmul,
     pin_gateup,
     pin_moe,
+    pin_silu,
+    pin_swiglu,
+    pin_topk_softmax,
+    pin_router,
 ]

@@ -14,6 +14,13 @@ import oracle_pins
 
 # (name, text in oracle.c, replacement)
 MUTATIONS = [
+    ("silu sign", "return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    ("swiglu uses u twice", "y[i] = oracle_silu(g[i]) * u[i];", "y[i] = oracle_silu(u[i]) * u[i];"),
+    ("top-k ties to the higher index", "if (best < 0 || lg[e] > lg[best]) best = e;",
+     "if (best < 0 || lg[e] >= lg[best]) best = e;"),
+    ("top-k weights not renormalised", "for (int64_t i = 0; i < topk; ++i) weights[i] /= s;",
+     "for (int64_t i = 0; i < topk; ++i) weights[i] /= 1.0;"),
+    ("softmax over the top-k only", "weights[i] = exp(lg[best] - mx) / z;", "weights[i] = exp(lg[best] - mx);"),
     ("q4 nibble halves swapped", "int q = (j < 16) ? (byte & 0x0F) : (byte >> 4);",
      "int q = (j < 16) ? (byte >> 4) : (byte & 0x0F);"),
     ("q4 sequential byte order", "qs_row[b * 16 + (j % 16)]", "qs_row[b * 16 + (j / 2)]"),

@@ -128,6 +128,22 @@ int moe_q4_gemv(float *y_gate, float *y_up, const uint8_t *qs_gate, const uint16
                 int K, int32_t *dev_status, q4_stream_t stream);
 
 /*
+ * SwiGLU epilogue variants (one output instead of two):
+ *   fused_gateup_swiglu_q4k_gemv: y[n] = silu(g[n]) * u[n] with g, u the two outputs of
+ *     fused_gateup_q4k_gemv (same arguments, same RMSNorm rule);
+ *   moe_q4_swiglu_gemv: y[(t*topk + s)*N + r] = silu(g) * u with g, u the two outputs of moe_q4_gemv for that
+ *     routed row (same arguments, same routing, NaN for an invalid id, same dev_status rule).
+ * silu(g) = g / (1 + exp(-g)). The pages show only that production MoE keeps one value per routed row; the
+ * gated-linear-unit form is the standard one. Each call reads every weight byte once, as the two-output forms.
+ *   y float[N] (gate+up) or float[T][topk][N] (MoE), 4-byte aligned.
+ */
+int fused_gateup_swiglu_q4k_gemv(float *y, const uint8_t *w_gate, const uint8_t *w_up, const float *x,
+                                 const float *gamma, float eps, int N, int K, q4_stream_t stream);
+int moe_q4_swiglu_gemv(float *y, const uint8_t *qs_gate, const uint16_t *d_gate, const uint8_t *qs_up,
+                       const uint16_t *d_up, const float *x, const int32_t *expert_ids, int T, int topk, int E,
+                       int N, int K, int32_t *dev_status, q4_stream_t stream);
+
+/*
  * Pure-read ceiling instruments: the same bytes, the same addressing and the same launch shape as the
  * matching GEMV, but no unpack and no dot products. Each output row receives the XOR of the 32-bit quant
  * words and zero-extended 16-bit scales (Q4) or of the 32-bit words of the super-blocks (Q4_K) of that

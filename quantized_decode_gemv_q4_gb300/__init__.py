@@ -22,7 +22,8 @@ from . import build as _build
 
 __all__ = [
     "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
-    "moe_q4_gemv", "q4_pure_read", "q4k_pure_read", "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
+    "moe_q4_gemv", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "q4_pure_read", "q4k_pure_read",
+    "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
     "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "FAULT_BAD_EXPERT",
 ]
 
@@ -52,6 +53,8 @@ _SIGNATURES = {
     "moe_q4_pure_read": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
     "q4_dequant": [_P, _P, _P, _I, _I, _P],
     "q4k_dequant": [_P, _P, _I, _I, _P],
+    "fused_gateup_swiglu_q4k_gemv": [_P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _P],
+    "moe_q4_swiglu_gemv": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
     "q4_device_faults": [ctypes.POINTER(ctypes.c_uint)],
 }
 
@@ -177,6 +180,28 @@ def moe_q4_gemv(y_gate, y_up, qs_gate, d_gate, qs_up, d_up, x, expert_ids, E: in
                               _ptr(qs_up, torch.uint8, "qs_up"), _ptr(d_up, torch.float16, "d_up"),
                               _ptr(x, torch.float32, "x"), _ptr(expert_ids, torch.int32, "expert_ids"),
                               T, topk, E, N, K, _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def fused_gateup_swiglu_q4k_gemv(y, w_gate, w_up, x, gamma=None, eps: float = 1e-5, stream=None) -> None:
+    """y = silu(W_gate xhat) * (W_up xhat), one output (xhat as fused_gateup_q4k_gemv)."""
+    N, K = _q4k_dims(w_gate)
+    if _q4k_dims(w_up) != (N, K) or x.numel() != K or y.numel() != N:
+        raise ValueError("w_gate and w_up must be [N, K/256, 144], x [K], y [N]")
+    _check(load().fused_gateup_swiglu_q4k_gemv(_ptr(y, torch.float32, "y"), _ptr(w_gate, torch.uint8, "w_gate"),
+                                               _ptr(w_up, torch.uint8, "w_up"), _ptr(x, torch.float32, "x"),
+                                               _ptr(gamma, torch.float32, "gamma"), float(eps), N, K, _stream(stream)))
+
+
+def moe_q4_swiglu_gemv(y, qs_gate, d_gate, qs_up, d_up, x, expert_ids, E: int, dev_status=None, stream=None) -> None:
+    """y[t, s] = silu(gate) * up for every routed row (routing as moe_q4_gemv)."""
+    T, topk, N, K = _moe_dims(qs_gate, d_gate, expert_ids, E)
+    if x.numel() != T * K or y.numel() != T * topk * N:
+        raise ValueError("x must be [T, K] and y [T, topk, N]")
+    _check(load().moe_q4_swiglu_gemv(_ptr(y, torch.float32, "y"), _ptr(qs_gate, torch.uint8, "qs_gate"),
+                                     _ptr(d_gate, torch.float16, "d_gate"), _ptr(qs_up, torch.uint8, "qs_up"),
+                                     _ptr(d_up, torch.float16, "d_up"), _ptr(x, torch.float32, "x"),
+                                     _ptr(expert_ids, torch.int32, "expert_ids"), T, topk, E, N, K,
+                                     _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def q4_pure_read(sink, qs, d, stream=None) -> None:

@@ -160,7 +160,7 @@ int fused_rmsnorm_q4k_gemv(float* y, const uint8_t* w, const float* x, const flo
     Q4_TRY(check_eps(what, eps));
     DeviceInfo di;
     Q4_TRY(check_device(what, &di));
-    return finish(what, launch_q4k_gemv(y, nullptr, w, nullptr, x, gamma, eps, N, K, (cudaStream_t)stream));
+    return finish(what, launch_q4k_gemv(y, nullptr, w, nullptr, x, gamma, eps, N, K, false, (cudaStream_t)stream));
 }
 
 int fused_gateup_q4k_gemv(float* y_gate, float* y_up, const uint8_t* w_gate, const uint8_t* w_up, const float* x,
@@ -175,7 +175,7 @@ int fused_gateup_q4k_gemv(float* y_gate, float* y_up, const uint8_t* w_gate, con
     Q4_TRY(check_eps(what, eps));
     DeviceInfo di;
     Q4_TRY(check_device(what, &di));
-    return finish(what, launch_q4k_gemv(y_gate, y_up, w_gate, w_up, x, gamma, eps, N, K, (cudaStream_t)stream));
+    return finish(what, launch_q4k_gemv(y_gate, y_up, w_gate, w_up, x, gamma, eps, N, K, false, (cudaStream_t)stream));
 }
 
 static int check_moe(const char* what, const float* y_gate, const float* y_up, const uint8_t* qs_gate,
@@ -205,7 +205,34 @@ int moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gate, const uint16
     DeviceInfo di;
     Q4_TRY(check_device(what, &di));
     return finish(what, launch_moe_q4_gemv(y_gate, y_up, qs_gate, d_gate, qs_up, d_up, x, expert_ids, T, topk, E, N,
-                                           K, dev_status, false, (cudaStream_t)stream));
+                                           K, dev_status, false, false, (cudaStream_t)stream));
+}
+
+int fused_gateup_swiglu_q4k_gemv(float* y, const uint8_t* w_gate, const uint8_t* w_up, const float* x,
+                                 const float* gamma, float eps, int N, int K, q4_stream_t stream) {
+    const char* what = "fused_gateup_swiglu_q4k_gemv";
+    Q4_TRY(check_out(what, y));
+    Q4_TRY(check_q4k_weights(what, w_gate, N, K));
+    Q4_TRY(check_q4k_weights(what, w_up, N, K));
+    Q4_TRY(check_vec(what, "x", x));
+    if (gamma) Q4_TRY(check_vec(what, "gamma", gamma));
+    Q4_TRY(check_eps(what, eps));
+    DeviceInfo di;
+    Q4_TRY(check_device(what, &di));
+    return finish(what, launch_q4k_gemv(y, nullptr, w_gate, w_up, x, gamma, eps, N, K, true, (cudaStream_t)stream));
+}
+
+int moe_q4_swiglu_gemv(float* y, const uint8_t* qs_gate, const uint16_t* d_gate, const uint8_t* qs_up,
+                       const uint16_t* d_up, const float* x, const int32_t* expert_ids, int T, int topk, int E, int N,
+                       int K, int32_t* dev_status, q4_stream_t stream) {
+    const char* what = "moe_q4_swiglu_gemv";
+    Q4_TRY(check_moe(what, y, y, qs_gate, d_gate, qs_up, d_up, expert_ids, T, topk, E, N, K));
+    Q4_TRY(check_vec(what, "x", x));
+    if (dev_status && !aligned(dev_status, 4)) return fail(Q4_EALIGN, "%s: dev_status must be 4-byte aligned", what);
+    DeviceInfo di;
+    Q4_TRY(check_device(what, &di));
+    return finish(what, launch_moe_q4_gemv(y, nullptr, qs_gate, d_gate, qs_up, d_up, x, expert_ids, T, topk, E, N, K,
+                                           dev_status, false, true, (cudaStream_t)stream));
 }
 
 int q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, q4_stream_t stream) {
@@ -235,7 +262,7 @@ int moe_q4_pure_read(float* sink_gate, float* sink_up, const uint8_t* qs_gate, c
     DeviceInfo di;
     Q4_TRY(check_device(what, &di));
     return finish(what, launch_moe_q4_gemv(sink_gate, sink_up, qs_gate, d_gate, qs_up, d_up, nullptr, expert_ids, T,
-                                           topk, E, N, K, dev_status, true, (cudaStream_t)stream));
+                                           topk, E, N, K, dev_status, true, false, (cudaStream_t)stream));
 }
 
 int q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, q4_stream_t stream) {

@@ -363,6 +363,9 @@ struct NextPow2 {
     static constexpr int value = X <= 1 ? 1 : X <= 2 ? 2 : X <= 4 ? 4 : X <= 8 ? 8 : X <= 16 ? 16 : 32;
 };
 
+// silu(g) = g / (1 + e^-g), the gate of the SwiGLU epilogue.
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
 }

@@ -42,7 +42,7 @@ constexpr int kMaxC = 4;        // routed slots served per weight sweep
 
 struct MoEParams {
     float* yg;
-    float* yu;
+    float* yu;  // nullptr in the SwiGLU form (one output)
     const uint8_t* qg;
     const uint16_t* dg;
     const uint8_t* qu;
@@ -79,13 +79,18 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-template <int R, int W, int D, int UPL, bool PURE>
+// SWIGLU: a job streams R gate rows and the same R up rows of its expert (one slot of 2R rows) and writes
+// silu(gate) * up per routed row; otherwise a job is R rows of one projection.
+template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
+    static_assert(!(PURE && SWIGLU), "the pure-read instrument streams one projection per job");
+    constexpr int NP = SWIGLU ? 1 : 2;      // jobs per (group, row group)
+    constexpr int RR = SWIGLU ? 2 * R : R;  // rows per slot
     constexpr int kThreads = W * 32;
     constexpr int CB = 32 * UPL;
     constexpr uint32_t QROW = CB * 16u;
-    constexpr uint32_t QBYTES = R * QROW;
-    constexpr uint32_t SLOT = moe_slot_bytes(R, UPL);
+    constexpr uint32_t QBYTES = RR * QROW;
+    constexpr uint32_t SLOT = moe_slot_bytes(RR, UPL);
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             if (owner[i] >= 0) continue;
             for (int r = threadIdx.x; r < p.N; r += kThreads) {
                 p.yg[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);
-                p.yu[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);
+                if constexpr (!SWIGLU) p.yu[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);  // no y_up
             }
             if (threadIdx.x == 0) {
                 if (p.status) atomicOr(reinterpret_cast<unsigned*>(p.status), (unsigned)kFaultBadExpert);
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
     const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
-    const int jobs = ngroups * 2 * rgs;
+    const int jobs = ngroups * NP * rgs;
     // Warps are numbered CTA by CTA, and the groups run in order of slot count, so the warps of one SM own
     // neighbouring job ranges and mostly run the same compiled stage body (one set of instructions hot).
     const int gw = (int)blockIdx.x * W + warp;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         long long cb = 0;
         for (int c0 = 0; c0 < ngroups; c0 += 32) {
             const int oi = c0 + lane;
-            long long v = oi < ngroups ? 2LL * rgs * job_cost(group_cnt[gorder[oi]] & 0xFF, PURE, p.cost_a, p.cost_b) : 0LL;
+            long long v = oi < ngroups ? (long long)NP * rgs * job_cost(group_cnt[gorder[oi]] & 0xFF, PURE, p.cost_a, p.cost_b) : 0LL;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const long long t = __shfl_up_sync(0xffffffffu, v, off);
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             if (gcum[mid] <= c) lo = mid;
             else hi = mid - 1;
         }
-        return lo * 2 * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]] & 0xFF, PURE, p.cost_a, p.cost_b));
+        return lo * NP * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]] & 0xFF, PURE, p.cost_a, p.cost_b));
     };
     const int j0 = job_at(total_cost * gw / Wtot);
     const int j1 = job_at(total_cost * (gw + 1) / Wtot);
@@ -278,8 +283,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     };
     auto cursor_at = [&](int j) {
         Cursor k;
-        k.grp = j / (2 * rgs);
-        const int rem = j - k.grp * 2 * rgs;
+        k.grp = j / (NP * rgs);
+        const int rem = j - k.grp * NP * rgs;
         k.sp = rem / rgs;
         k.rg = rem - k.sp * rgs;
         k.c = 0;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             k.c = 0;
             if (++k.rg == rgs) {
                 k.rg = 0;
-                if (++k.sp == 2) {
+                if (++k.sp == NP) {
                     k.sp = 0;
                     ++k.grp;
                 }
@@ -308,19 +313,25 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             const int rv = min(R, p.N - r0);
             const int b0 = ik.c * CB;
             const int nb = min(CB, p.nblk - b0);
-            const uint8_t* q = ik.sp == 0 ? p.qg : p.qu;
-            const uint16_t* d = ik.sp == 0 ? p.dg : p.du;
             const size_t row0 = (size_t)e * p.N + r0;
             const uint32_t slot = ring + (uint32_t)islot * SLOT;
-            if (nb == CB && p.S == 1) {
-                warp_copy_async(slot, q + row0 * QROW, (uint32_t)rv * QROW, lane, pol);
-                if (p.dcopy) warp_copy_async(slot + QBYTES, d + row0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
-            } else {
-                for (int r = 0; r < rv; ++r) {
-                    const size_t rb = (row0 + r) * p.nblk + b0;
-                    warp_copy_async(slot + (uint32_t)r * QROW, q + rb * 16, (uint32_t)(nb * 16), lane, pol);
-                    if (p.dcopy)
-                        warp_copy_async(slot + QBYTES + (uint32_t)(r * CB * 2), d + rb, (uint32_t)(nb * 2), lane, pol);
+#pragma unroll
+            for (int sp = 0; sp < (SWIGLU ? 2 : 1); ++sp) {
+                const int proj = SWIGLU ? sp : ik.sp;
+                const uint8_t* q = proj == 0 ? p.qg : p.qu;
+                const uint16_t* d = proj == 0 ? p.dg : p.du;
+                const uint32_t qdst = slot + (uint32_t)(sp * R) * QROW;
+                const uint32_t ddst = slot + QBYTES + (uint32_t)(sp * R * CB * 2);
+                if (nb == CB && p.S == 1) {
+                    warp_copy_async(qdst, q + row0 * QROW, (uint32_t)rv * QROW, lane, pol);
+                    if (p.dcopy) warp_copy_async(ddst, d + row0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
+                } else {
+                    for (int r = 0; r < rv; ++r) {
+                        const size_t rb = (row0 + r) * p.nblk + b0;
+                        warp_copy_async(qdst + (uint32_t)r * QROW, q + rb * 16, (uint32_t)(nb * 16), lane, pol);
+                        if (p.dcopy)
+                            warp_copy_async(ddst + (uint32_t)(r * CB * 2), d + rb, (uint32_t)(nb * 2), lane, pol);
+                    }
                 }
             }
             advance(ik);
@@ -374,10 +385,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     __syncthreads();
 
     const uint32_t qstride = (uint32_t)U * 16u;  // bytes between the quads of one unit
-    float tot[R][kMaxC];
-    uint32_t fold[R];
+    float tot[RR][kMaxC];
+    uint32_t fold[RR];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int r = 0; r < RR; ++r) {
         fold[r] = 0u;
 #pragma unroll
         for (int m = 0; m < kMaxC; ++m) tot[r][m] = 0.f;
@@ -399,7 +410,6 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         const int rv = min(R, p.N - r0);
         const int b0 = k.c * CB;
         const int nb = min(CB, p.nblk - b0);
-        const uint16_t* dglob = k.sp == 0 ? p.dg : p.du;
         const uint32_t qb = slot + (uint32_t)lane * 16u;
         const uint32_t db = slot + QBYTES + (uint32_t)lane * 2u;
 
@@ -414,38 +424,42 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                 const int ul = it * 32 + lane;
                 if (ul >= nb) continue;
                 const uint32_t u = (uint32_t)(b0 + ul);
-                uint4 w[R];
-                float dsc[R];
-                uint32_t dbits[R];
+                uint4 w[RR];
+                float dsc[RR];
+                uint32_t dbits[RR];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
+                for (int r = 0; r < RR; ++r) {
+                    // slot row r: projection (SWIGLU ? r / R : k.sp), expert row r0 + r % R
+                    const int rr = SWIGLU ? r % R : r;
                     w[r] = lds128(qb + (uint32_t)r * QROW + (uint32_t)(it * 512));
-                    if (p.dcopy)
+                    if (p.dcopy) {
                         dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
-                    else
-                        dbits[r] = r < rv ? (uint32_t)__ldg(dglob + ((size_t)e * p.N + r0 + r) * p.nblk + u) : 0u;
+                    } else {
+                        const uint16_t* dglob = (SWIGLU ? r >= R : k.sp != 0) ? p.du : p.dg;
+                        dbits[r] = rr < rv ? (uint32_t)__ldg(dglob + ((size_t)e * p.N + r0 + rr) * p.nblk + u) : 0u;
+                    }
                     dsc[r] = f16_bits_to_f32(dbits[r]);
                 }
                 if constexpr (PURE) {
 #pragma unroll
-                    for (int r = 0; r < R; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
+                    for (int r = 0; r < RR; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
                 } else {
                     uint32_t xa[C];
 #pragma unroll
                     for (int m = 0; m < C; ++m) xa[m] = xs + ((uint32_t)tok[m] * 8u * (uint32_t)U + u) * 16u;
-                    float2 acc[R][C];
+                    float2 acc[RR][C];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        Word8s d8[R];
+                        Word8s d8[RR];
 #pragma unroll
-                        for (int r = 0; r < R; ++r)
+                        for (int r = 0; r < RR; ++r)
                             d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
 #pragma unroll
                         for (int m = 0; m < C; ++m) {
                             const float4 xl = lds128f(xa[m] + (uint32_t)i * qstride);
                             const float4 xh = lds128f(xa[m] + (uint32_t)(4 + i) * qstride);
 #pragma unroll
-                            for (int r = 0; r < R; ++r) {
+                            for (int r = 0; r < RR; ++r) {
                                 float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][m];
                                 a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
                                 a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     for (int m = 0; m < C; ++m) {
                         const float2 fa = lds64f(aux + ((uint32_t)tok[m] * (uint32_t)U + u) * 8u);
 #pragma unroll
-                        for (int r = 0; r < R; ++r) {
+                        for (int r = 0; r < RR; ++r) {
                             const float t = fmaf(acc[r][m].x + acc[r][m].y, fa.x, fa.y);
                             tot[r][m] = fmaf(dsc[r], t, tot[r][m]);
                         }
@@ -470,6 +484,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 
             if (k.c == p.S - 1) {
                 float* y = k.sp == 0 ? p.yg : p.yu;
+                (void)y;
                 if constexpr (PURE) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -479,14 +494,14 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                         fold[r] = 0u;
                     }
                 } else {
-                    constexpr int NV = R * C;
+                    constexpr int NV = RR * C;
                     constexpr int P2 = NextPow2<NV>::value;
                     constexpr int L2 = log2_const<P2>();
                     float vals[P2];
 #pragma unroll
                     for (int i = 0; i < P2; ++i) vals[i] = 0.f;
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
+                    for (int r = 0; r < RR; ++r)
 #pragma unroll
                         for (int m = 0; m < C; ++m) {
                             vals[r * C + m] = tot[r][m];
@@ -495,7 +510,15 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     warp_transpose_reduce<P2>(vals, lane);
                     const int idx = lane >> (5 - L2);
                     const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
-                    if (leader && idx < NV) {
+                    if constexpr (SWIGLU) {
+                        // the up total of (row r, slot m) sits R*C lane groups after its gate total
+                        const float up = __shfl_down_sync(0xffffffffu, vals[0], (R * C) << (5 - L2));
+                        if (leader && idx < R * C) {
+                            const int r = idx / C;
+                            const int m = idx - r * C;
+                            if (r < rv) p.yg[(size_t)list[first + m] * p.N + r0 + r] = silu(vals[0]) * up;
+                        }
+                    } else if (leader && idx < NV) {
                         const int r = idx / C;
                         const int m = idx - r * C;
                         if (r < rv) y[(size_t)list[first + m] * p.N + r0 + r] = vals[0];
@@ -548,7 +571,7 @@ unsigned* fault_word(int device) {
     return ptrs[device & 63];
 }
 
-template <int R, int W, int D, int UPL, bool PURE>
+template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     const uint32_t route = (uint32_t)round_up(kRouteInts * 4, 128);
     const uint32_t xsb = PURE ? 0u : (uint32_t)round_up(p.T * p.K * 4, 128);
@@ -557,10 +580,10 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     p.xs_off = route;
     p.aux_off = route + xsb;
     p.slots_off = route + xsb + axb;
-    const uint32_t smem = p.slots_off + (uint32_t)(W * D) * moe_slot_bytes(R, UPL);
+    const uint32_t smem = p.slots_off + (uint32_t)(W * D) * moe_slot_bytes(SWIGLU ? 2 * R : R, UPL);
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     p.S = (p.nblk + 32 * UPL - 1) / (32 * UPL);
-    auto kern = moe_q4_kernel<R, W, D, UPL, PURE>;
+    auto kern = moe_q4_kernel<R, W, D, UPL, PURE, SWIGLU>;
     static std::once_flag attr_once[64];
     cudaError_t err = cudaSuccess;
     std::call_once(attr_once[di.device & 63], [&] {
@@ -570,24 +593,24 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     return launch_kernel(kern, di.sm_count, W * 32, smem, s, p);
 }
 
-template <int R, int W, int UPL, bool PURE>
+template <int R, int W, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_upl(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
-    if (depth >= 4) e = launch_fixed<R, W, 4, UPL, PURE>(di, p, s);
-    if (e == cudaErrorNotSupported && depth >= 3) e = launch_fixed<R, W, 3, UPL, PURE>(di, p, s);
-    if (e == cudaErrorNotSupported) e = launch_fixed<R, W, 2, UPL, PURE>(di, p, s);
+    if (depth >= 4) e = launch_fixed<R, W, 4, UPL, PURE, SWIGLU>(di, p, s);
+    if (e == cudaErrorNotSupported && depth >= 3) e = launch_fixed<R, W, 3, UPL, PURE, SWIGLU>(di, p, s);
+    if (e == cudaErrorNotSupported) e = launch_fixed<R, W, 2, UPL, PURE, SWIGLU>(di, p, s);
     return e;
 }
 
 // Whole rows in one chunk up to K = 4096 (UPL = 1, 2, 4), longer rows in 128-block chunks; the deepest ring
 // that fits beside the routing tables and the staged tokens.
-template <int R, int W, bool PURE>
+template <int R, int W, bool PURE, bool SWIGLU = false>
 cudaError_t launch(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
-    if (p.nblk <= 32) e = launch_upl<R, W, 1, PURE>(di, p, depth, s);
-    else if (p.nblk <= 64) e = launch_upl<R, W, 2, PURE>(di, p, depth, s);
-    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 4, PURE>(di, p, depth, s);
-    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 1, PURE>(di, p, depth, s);
+    if (p.nblk <= 32) e = launch_upl<R, W, 1, PURE, SWIGLU>(di, p, depth, s);
+    else if (p.nblk <= 64) e = launch_upl<R, W, 2, PURE, SWIGLU>(di, p, depth, s);
+    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 4, PURE, SWIGLU>(di, p, depth, s);
+    if (e == cudaErrorNotSupported) e = launch_upl<R, W, 1, PURE, SWIGLU>(di, p, depth, s);
     return e;
 }
 
@@ -596,7 +619,7 @@ cudaError_t launch(const DeviceInfo& di, const MoEParams& p, int depth, cudaStre
 cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gate, const uint16_t* d_gate,
                                const uint8_t* qs_up, const uint16_t* d_up, const float* x, const int32_t* ids,
                                int T, int topk, int E, int N, int K, int32_t* dev_status, bool pure_read,
-                               cudaStream_t s) {
+                               bool swiglu, cudaStream_t s) {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
@@ -625,6 +648,11 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.cost_b = 5;
     plan_override(&variant, &depth, &p.cost_a, &p.cost_b);
     if (pure_read) return variant == 216 ? launch<2, 16, true>(di, p, depth, s) : launch<4, 8, true>(di, p, depth, s);
+    if (swiglu) {  // R gate + R up rows per slot
+        if (variant == 216) return launch<1, 16, false, true>(di, p, depth, s);
+        if (variant == 84) return launch<4, 8, false, true>(di, p, depth, s);
+        return launch<2, 8, false, true>(di, p, depth, s);
+    }
     return variant == 216 ? launch<2, 16, false>(di, p, depth, s) : launch<4, 8, false>(di, p, depth, s);
 }
 

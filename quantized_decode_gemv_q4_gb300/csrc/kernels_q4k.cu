@@ -40,6 +40,7 @@ struct Q4KParams {
     const float* x;
     const float* gamma;  // nullptr: no RMSNorm
     float eps;
+    int swiglu;          // two streams only: y0 = silu(gate) * up, y1 unused
     int N, K, nsb;
     int CS;           // super-blocks per chunk
     int S;            // chunks per row
@@ -311,7 +312,11 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_gemv_kernel(const Q4KParams p) 
                 warp_transpose_reduce<P2>(vals, lane);
                 const int idx = lane >> (5 - L2);
                 const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
-                if (leader && idx < NV) {
+                if (NS == 2 && p.swiglu) {
+                    // row rr's up total sits R lane groups after its gate total
+                    const float up = __shfl_down_sync(0xffffffffu, vals[0], R << (5 - L2));
+                    if (leader && idx < R && idx < rv) p.y0[r0 + idx] = silu(vals[0]) * up;
+                } else if (leader && idx < NV) {
                     const int s = idx / R;
                     const int rr = idx - s * R;
                     if (rr < rv) (s == 0 ? p.y0 : p.y1)[r0 + rr] = vals[0];
@@ -395,6 +400,7 @@ struct Args {
     const float *x, *gamma;
     float eps;
     int N, K;
+    bool swiglu;
 };
 
 template <int NS, int R, int W, int D, bool PURE>
@@ -448,6 +454,7 @@ cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t
     p.x = a.x;
     p.gamma = a.gamma;
     p.eps = a.eps;
+    p.swiglu = a.swiglu ? 1 : 0;
     p.N = a.N;
     p.K = a.K;
     p.nsb = nsb;
@@ -463,11 +470,11 @@ cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t
 }  // namespace
 
 cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
-                            const float* gamma, float eps, int N, int K, cudaStream_t s) {
+                            const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s) {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
-    const Args a{y0, y1, w0, w1, x, gamma, eps, N, K};
+    const Args a{y0, y1, w0, w1, x, gamma, eps, N, K, swiglu && w1 != nullptr};
     int cs = 16, depth = 2, variant = 1;
     plan_override(&cs, &depth, &variant);
     if (w1) {
@@ -483,7 +490,7 @@ cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cu
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
-    const Args a{sink, nullptr, w, nullptr, nullptr, nullptr, 0.f, N, K};
+    const Args a{sink, nullptr, w, nullptr, nullptr, nullptr, 0.f, N, K, false};
     int cs = 16, depth = 2, variant = 1;
     plan_override(&cs, &depth, &variant);
     return run<1, 2, 16, true>(di, a, cs, depth, s);

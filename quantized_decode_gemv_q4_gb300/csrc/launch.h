@@ -47,17 +47,19 @@ cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* 
 cudaError_t launch_q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 
 // ---- Q4_K (144-byte super-blocks of 256 weights) ------------------------------------------------------
-// One or two weight streams against one input; gamma == nullptr skips RMSNorm.
+// One or two weight streams against one input; gamma == nullptr skips RMSNorm. With swiglu (two streams)
+// y0 = silu(W0 xhat) * (W1 xhat) and y1 is not written.
 cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
-                            const float* gamma, float eps, int N, int K, cudaStream_t s);
+                            const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s);
 cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s);
 cudaError_t launch_q4k_dequant(float* W, const uint8_t* w, int N, int K, cudaStream_t s);
 
 // ---- MoE expert-gathered planar Q4 gate+up ---------------------------------------------------------
+// swiglu: y_gate = silu(gate) * up per routed row, y_up unused.
 cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gate, const uint16_t* d_gate,
                                const uint8_t* qs_up, const uint16_t* d_up, const float* x, const int32_t* ids,
                                int T, int topk, int E, int N, int K, int32_t* dev_status, bool pure_read,
-                               cudaStream_t s);
+                               bool swiglu, cudaStream_t s);
 
 // ---- device fault word (set by the MoE kernels on an expert id outside [0, E)) --------------------
 cudaError_t read_and_clear_fault_moe(unsigned* out);

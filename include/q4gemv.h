@@ -144,6 +144,24 @@ int moe_q4_swiglu_gemv(float *y, const uint8_t *qs_gate, const uint16_t *d_gate,
                        int N, int K, int32_t *dev_status, q4_stream_t stream);
 
 /*
+ * MoE router: gate GEMV over the experts fused with top-K softmax, for the decode tokens of one step.
+ * Source: spark_model gemm_quant.rs, moe_gate_topk_fused (gate[e] = x . Wgate[e] for every expert, then the
+ * top-K indices and softmax weights, `normalize` flag). Here the router rows are planar Q4 (the library's
+ * format) and the inputs fp32. For token t < T:
+ *   logits[t][e] = sum_k Wr[e][k] * x[t][k] for e < E (written when logits != NULL);
+ *   expert_ids[t][i], i < topk: the experts of the topk largest logits in descending order, ties to the lower
+ *     index (a NaN logit ranks below every other);
+ *   expert_weights[t][i] = softmax over all E logits at expert_ids[t][i], divided by the sum over the topk
+ *     picks when normalize != 0.
+ * The ids can be passed straight to moe_q4_gemv / moe_q4_swiglu_gemv (same [T][topk] layout).
+ *   expert_ids int32[T][topk], expert_weights float[T][topk], logits float[T][E] or NULL (4-byte aligned);
+ *   qs uint8[E][K/32][16], d uint16[E][K/32] as q4_gemv; x float[T][K] (16-byte aligned).
+ *   1 <= E <= 4096; 1 <= topk <= E; T >= 1; K % 32 == 0.
+ */
+int moe_router_q4(int32_t *expert_ids, float *expert_weights, float *logits, const uint8_t *qs, const uint16_t *d,
+                  const float *x, int T, int E, int K, int topk, int normalize, q4_stream_t stream);
+
+/*
  * Pure-read ceiling instruments: the same bytes, the same addressing and the same launch shape as the
  * matching GEMV, but no unpack and no dot products. Each output row receives the XOR of the 32-bit quant
  * words and zero-extended 16-bit scales (Q4) or of the 32-bit words of the super-blocks (Q4_K) of that

@@ -22,7 +22,8 @@ from . import build as _build
 
 __all__ = [
     "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
-    "moe_q4_gemv", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "q4_pure_read", "q4k_pure_read",
+    "moe_q4_gemv", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "moe_router_q4", "q4_pure_read",
+    "q4k_pure_read",
     "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
     "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "FAULT_BAD_EXPERT",
 ]
@@ -55,6 +56,7 @@ _SIGNATURES = {
     "q4k_dequant": [_P, _P, _I, _I, _P],
     "fused_gateup_swiglu_q4k_gemv": [_P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _P],
     "moe_q4_swiglu_gemv": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
+    "moe_router_q4": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "q4_device_faults": [ctypes.POINTER(ctypes.c_uint)],
 }
 
@@ -202,6 +204,22 @@ def moe_q4_swiglu_gemv(y, qs_gate, d_gate, qs_up, d_up, x, expert_ids, E: int, d
                                      _ptr(d_up, torch.float16, "d_up"), _ptr(x, torch.float32, "x"),
                                      _ptr(expert_ids, torch.int32, "expert_ids"), T, topk, E, N, K,
                                      _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def moe_router_q4(expert_ids, expert_weights, qs, d, x, topk: int, normalize: bool = True, logits=None,
+                  stream=None) -> None:
+    """Router logits of E planar-Q4 rows for T tokens, then the top-K experts and their softmax weights."""
+    E, K = _q4_dims(qs, d)
+    T = x.numel() // K
+    if x.numel() != T * K or expert_ids.numel() != T * topk or expert_weights.numel() != T * topk:
+        raise ValueError("x must be [T, K], expert_ids and expert_weights [T, topk]")
+    if logits is not None and logits.numel() != T * E:
+        raise ValueError("logits must be [T, E]")
+    _check(load().moe_router_q4(_ptr(expert_ids, torch.int32, "expert_ids"),
+                                _ptr(expert_weights, torch.float32, "expert_weights"),
+                                _ptr(logits, torch.float32, "logits"), _ptr(qs, torch.uint8, "qs"),
+                                _ptr(d, torch.float16, "d"), _ptr(x, torch.float32, "x"), T, E, K, topk,
+                                1 if normalize else 0, _stream(stream)))
 
 
 def q4_pure_read(sink, qs, d, stream=None) -> None:

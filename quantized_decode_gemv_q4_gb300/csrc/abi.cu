@@ -235,6 +235,23 @@ int moe_q4_swiglu_gemv(float* y, const uint8_t* qs_gate, const uint16_t* d_gate,
                                            dev_status, false, true, (cudaStream_t)stream));
 }
 
+int moe_router_q4(int32_t* expert_ids, float* expert_weights, float* logits, const uint8_t* qs, const uint16_t* d,
+                  const float* x, int T, int E, int K, int topk, int normalize, q4_stream_t stream) {
+    const char* what = "moe_router_q4";
+    if (!expert_ids || !expert_weights) return fail(Q4_EINVAL, "%s: null output pointer", what);
+    if (!aligned(expert_ids, 4) || !aligned(expert_weights, 4) || (logits && !aligned(logits, 4)))
+        return fail(Q4_EALIGN, "%s: outputs must be 4-byte aligned", what);
+    if (E <= 0 || E > 4096) return fail(Q4_EINVAL, "%s: E must be in 1..4096 (got %d)", what, E);
+    Q4_TRY(check_q4_weights(what, qs, d, E, K));
+    Q4_TRY(check_vec(what, "x", x));
+    if (T <= 0) return fail(Q4_EINVAL, "%s: T must be >= 1 (got %d)", what, T);
+    if (topk <= 0 || topk > E) return fail(Q4_EINVAL, "%s: topk must be in 1..E (got %d, E=%d)", what, topk, E);
+    DeviceInfo di;
+    Q4_TRY(check_device(what, &di));
+    return finish(what, launch_moe_router(expert_ids, expert_weights, logits, qs, d, x, T, E, K, topk, normalize != 0,
+                                          (cudaStream_t)stream));
+}
+
 int q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, q4_stream_t stream) {
     const char* what = "q4_pure_read";
     Q4_TRY(check_out(what, sink));

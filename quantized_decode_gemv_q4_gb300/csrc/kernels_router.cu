@@ -1,0 +1,204 @@
+// MoE router for sm_103a: gate GEMV over the experts + top-K softmax, fused in one kernel.
+//
+// Problem (spark_model `gemm_quant.rs`, moe_gate_topk_fused): gate[e] = x . Wgate[e] for every expert, then the
+// indices of the K largest logits and their softmax weights (optionally renormalised over the K). Here Wgate is
+// planar Q4 (E rows of K weights, the library's format) and x is fp32; one token per CTA row of the grid.
+//
+// Kernel shape (one CTA of W warps per token; the router matrix is small and stays in L2 after the first CTA):
+//  * stage the token's x block by block with the bias-free decode's per-block scaling (device_common.cuh);
+//  * warp w computes the logits of experts w, w + W, ...: lane l takes units l, l + 32, ... of the row with
+//    16-byte loads, one shift + eight ANDs per word and packed fp32x2 FMAs, folds each block with its scale,
+//    and the warp sums the lanes; logits go to shared memory;
+//  * warp 0 takes the softmax over all E logits (max subtracted) and K arg-max passes (ties to the lower
+//    index), writes ids and weights (and, when asked, the logits).
+#include <algorithm>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace q4 {
+
+namespace {
+
+struct RouterParams {
+    int32_t* ids;
+    float* weights;
+    float* logits;  // nullable
+    const uint8_t* qs;
+    const uint16_t* d;
+    const float* x;
+    int T, E, K, nblk, topk, normalize;
+    uint32_t xs_off, aux_off, lg_off;
+};
+
+template <int W>
+__global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t xs = s_base + p.xs_off;
+    const uint32_t aux = s_base + p.aux_off;
+    float* lg = reinterpret_cast<float*>(smem + p.lg_off);
+
+    // x belongs to the previous kernel in the stream when launches overlap.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // stage x[t]: four lanes per 32-element block (whole warps take part in the group shuffles)
+    {
+        const float* xt = p.x + (size_t)t * p.K;
+        const int t4 = lane & 3;
+        const int nthr = (p.nblk * 4 + 31) & ~31;
+        for (int thr = threadIdx.x; thr < nthr; thr += W * 32) {
+            const int blk = thr >> 2;
+            const bool in = blk < p.nblk;
+            const float4* src = reinterpret_cast<const float4*>(xt) + (size_t)blk * 8 + 2 * t4;
+            const float4 a = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const Stage4 st = stage_block4(a, b, t4 >> 1);
+            if (in) {
+                const uint32_t a0 = xs + xs_chunk_offset(0u, (uint32_t)(2 * t4), (uint32_t)blk, 1u);
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y), "f"(st.a.z),
+                             "f"(st.a.w)
+                             : "memory");
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 512u), "f"(st.b.x), "f"(st.b.y),
+                             "f"(st.b.z), "f"(st.b.w)
+                             : "memory");
+                if (t4 == 0)
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset(0u, (uint32_t)blk, 1u)),
+                                 "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
+                                 : "memory");
+            }
+        }
+    }
+    __syncthreads();
+
+    // logits
+    for (int e = warp; e < p.E; e += W) {
+        float tot = 0.f;
+        for (int u = lane; u < p.nblk; u += 32) {
+            const size_t blk = (size_t)e * p.nblk + u;
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.qs) + blk);
+            const float dsc = f16_bits_to_f32(__ldg(p.d + blk));
+            const uint32_t xa = xs + xs_chunk_offset(0u, 0u, (uint32_t)u, 1u);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const Word8s d8 = decode_word_sub(i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w);
+                const float4 xl = lds128f(xa + (uint32_t)i * 512u);
+                const float4 xh = lds128f(xa + (uint32_t)(4 + i) * 512u);
+                acc = ffma2(d8.lo01, make_float2(xl.x, xl.y), acc);
+                acc = ffma2(d8.lo23, make_float2(xl.z, xl.w), acc);
+                acc = ffma2(d8.hi01, make_float2(xh.x, xh.y), acc);
+                acc = ffma2(d8.hi23, make_float2(xh.z, xh.w), acc);
+            }
+            const float2 fa = lds64f(aux + aux_offset(0u, (uint32_t)u, 1u));
+            tot = fmaf(dsc, fmaf(acc.x + acc.y, fa.x, fa.y), tot);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        if (lane == 0) {
+            if (p.logits) p.logits[(size_t)t * p.E + e] = tot;
+            lg[e] = tot != tot ? -INFINITY : tot;  // a NaN logit ranks last
+        }
+    }
+    __syncthreads();
+
+    // softmax over all E logits and the top K (warp 0)
+    if (warp == 0) {
+        float mx = -INFINITY;
+        for (int e = lane; e < p.E; e += 32) mx = fmaxf(mx, lg[e]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float z = 0.f;
+        for (int e = lane; e < p.E; e += 32) z += expf(lg[e] - mx);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        // K arg-max passes over the untaken experts (a taken expert's logit becomes NaN, which never compares
+        // greater or equal); ties go to the lower index. At most K-1 <= E-1 are taken, so a pass always finds one.
+        float wsum = 0.f;
+        float wsel = 0.f;
+        int isel = 0;
+        for (int i = 0; i < p.topk; ++i) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int e = lane; e < p.E; e += 32) {
+                const float v = lg[e];
+                if (v > bv || (v == bv && e < bi)) {
+                    bv = v;
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            const float pw = expf(bv - mx) / z;
+            wsum += pw;
+            if (lane == i % 32) {  // lane j holds pick j of the current group of 32 picks
+                wsel = pw;
+                isel = bi;
+            }
+            if (lane == 0) lg[bi] = __int_as_float(0x7fc00000);
+            __syncwarp();
+            if (i % 32 == 31 || i == p.topk - 1) {
+                const int base = i - (i % 32);
+                if (lane <= i % 32) {
+                    p.ids[(size_t)t * p.topk + base + lane] = isel;
+                    p.weights[(size_t)t * p.topk + base + lane] = wsel;  // renormalised below when asked
+                }
+            }
+        }
+        if (p.normalize) {
+            __syncwarp();
+            for (int i = lane; i < p.topk; i += 32) p.weights[(size_t)t * p.topk + i] /= wsum;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const uint8_t* qs, const uint16_t* d,
+                              const float* x, int T, int E, int K, int topk, bool normalize, cudaStream_t s) {
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess) return e;
+    constexpr int W = 8;
+    RouterParams p;
+    p.ids = ids;
+    p.weights = weights;
+    p.logits = logits;
+    p.qs = qs;
+    p.d = d;
+    p.x = x;
+    p.T = T;
+    p.E = E;
+    p.K = K;
+    p.nblk = K / 32;
+    p.topk = topk;
+    p.normalize = normalize ? 1 : 0;
+    const uint32_t xsb = xs_chunk_bytes(1u, (uint32_t)p.nblk);
+    const uint32_t axb = aux_bytes(1u, (uint32_t)p.nblk);
+    p.xs_off = 0;
+    p.aux_off = xsb;
+    p.lg_off = xsb + axb;
+    const uint32_t smem = p.lg_off + (uint32_t)E * 4u;
+    if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
+    auto kern = moe_router_kernel<W>;
+    static std::once_flag attr_once[64];
+    std::call_once(attr_once[di.device & 63], [&] {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+    });
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, T, W * 32, smem, s, p);
+}
+
+}  // namespace q4

@@ -61,6 +61,10 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
                                int T, int topk, int E, int N, int K, int32_t* dev_status, bool pure_read,
                                bool swiglu, cudaStream_t s);
 
+// ---- MoE router: gate GEMV over E planar-Q4 rows + top-K softmax per token ---------------------------
+cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const uint8_t* qs, const uint16_t* d,
+                              const float* x, int T, int E, int K, int topk, bool normalize, cudaStream_t s);
+
 // ---- device fault word (set by the MoE kernels on an expert id outside [0, E)) --------------------
 cudaError_t read_and_clear_fault_moe(unsigned* out);
 

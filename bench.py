@@ -34,7 +34,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = ["device_common.cuh", "launch.h", "q4_dense.cuh", "kernels_q4.cu", "kernels_q4_v2_4.cu",
-                  "kernels_q4_v5_8.cu", "kernels_q4k.cu", "kernels_moe.cu"]
+                  "kernels_q4_v5_8.cu", "kernels_q4k.cu", "kernels_moe.cu", "kernels_router.cu"]
 
 
 # ------------------------------------------------------------------------------------------------
@@ -436,6 +436,9 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes": table[dom][1], "us_per_launch": round(float(kt_us[dom]), 3)}
 
+    # ---- SURVEY NEXT rows, timed the same way but outside the headline step ------------------------------
+    next_rows = measure_next_rows(suite, inputs, stream, replicas, peak)
+
     # ---- end to end through the Python API with host buffers ---------------------------------------
     e2e = run_e2e(suite, inputs, stream, max(20, min(args.steps // 20, 400)), table)
 
@@ -458,7 +461,7 @@ def run_gpu(args):
                                          "overlap the previous call's tail)",
                        "value_without_launch_overlap": round(value_plain, 1),
                        "parallelism": f"replicas x{world}"},
-            "per_call": per_call, "roofline": roofline, "gpu_launches": args.steps * n_calls,
+            "per_call": per_call, "next_rows": next_rows, "roofline": roofline, "gpu_launches": args.steps * n_calls,
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -467,6 +470,73 @@ def run_gpu(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def _graph_us(fns, stream, reps=16, tries=5):
+    """Best per-launch device time of a graph of `reps` calls (fns rotated), after one replay."""
+    import torch
+
+    g = capture([fns[i % len(fns)] for i in range(reps)], stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    best = float("inf")
+    for _ in range(tries):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            g.replay()
+            b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b) / reps * 1e3)
+    del g
+    return best
+
+
+def measure_next_rows(suite, inputs, stream, replicas, peak):
+    """The router, the SwiGLU forms and a dependent router -> MoE-SwiGLU chain on the suite's workloads."""
+    import torch
+
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    dev = suite.x1.device
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    rng = np.random.default_rng(7)
+    E, K, T, topk = 64, 2048, 8, 8
+    rq, rd = synth.q4_weights(rng, E, K)  # router rows (73.7 KB: L2-resident, so latency-bound)
+    rq, rd = cu(rq), cu(rd)
+    ids = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, topk, device=dev)
+    ysw = torch.empty(18944, device=dev)
+    ymo = torch.empty(T, topk, 1408, device=dev)
+    c3eps = float(inputs[2]["eps"])
+    out = {}
+    us = _graph_us([lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, topk, True)], stream)
+    out["moe_router_q4 e64 k2048 t8 top8"] = {"us": round(us, 3)}
+    gb = 2 * q4k_bytes(18944, 3584)
+    us = _graph_us([lambda s=s: q4.fused_gateup_swiglu_q4k_gemv(ysw, suite.sets[s]["c3"][0], suite.sets[s]["c3"][1],
+                                                                suite.x3, suite.g3, c3eps) for s in range(replicas)],
+                   stream)
+    out["fused_gateup_swiglu_q4k_gemv 2x18944x3584"] = {"us": round(us, 3), "weight_GBps": round(gb / us / 1e3, 1),
+                                                        "frac_of_hbm_peak": round(gb / us / 1e3 / peak, 4)}
+    uniq = len(np.unique(inputs[4]["ids"]))
+    mb = 2 * uniq * q4_bytes(1408, 2048)
+    us = _graph_us([lambda s=s: q4.moe_q4_swiglu_gemv(ymo, *suite.sets[s]["c5"], suite.x5, suite.ids5, 64)
+                    for s in range(replicas)], stream)
+    out[f"moe_q4_swiglu_gemv e64 1408x2048 t8k8 ({uniq} experts)"] = {
+        "us": round(us, 3), "weight_GBps": round(mb / us / 1e3, 1), "frac_of_hbm_peak": round(mb / us / 1e3 / peak, 4)}
+    # dependent chain: the router's ids drive the MoE call on the device
+    chain = []
+    for ov in (True, False):
+        q4.q4_set_launch_overlap(ov)
+        fns = []
+        for s in range(replicas):
+            fns.append(lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, topk, True))
+            fns.append(lambda s=s: q4.moe_q4_swiglu_gemv(ymo, *suite.sets[s]["c5"], suite.x5, ids, 64))
+        chain.append(_graph_us(fns, stream, reps=16) * 2)
+    q4.q4_set_launch_overlap(True)
+    out["chain router -> moe_q4_swiglu_gemv (us per pair)"] = {"with_launch_overlap": round(chain[0], 3),
+                                                               "without": round(chain[1], 3)}
+    return out
 
 
 def run_e2e(suite, inputs, stream, steps, table):

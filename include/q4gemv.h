@@ -10,7 +10,7 @@
  *    as soon as the work is enqueued. Inputs must stay valid and unmodified until the work completes.
  *  - Return value: Q4_OK (0) when the work was enqueued, otherwise a negative code; nothing is enqueued when
  *    an argument is refused. The library refuses out-of-range arguments instead of clamping them.
- *      Q4_EINVAL       null required pointer, a size <= 0, M outside 1..8, K not a multiple of the block
+ *      Q4_EINVAL       null required pointer, a size <= 0, M outside 1..16, K not a multiple of the block
  *                      size (32 for Q4, 256 for Q4_K), topk > E, eps negative or not finite
  *      Q4_EALIGN       a pointer below the alignment stated for it
  *      Q4_ECUDA        a CUDA call failed (launch error, no device, ...)
@@ -82,10 +82,13 @@ int q4_gemv(float *y, const uint8_t *qs, const uint16_t *d, const float *x, int 
 
 /*
  * Y[m][n] = sum_k W[n][k] * X[m][k] for m < M, reading every weight byte once for all M rows.
- * Source: spark_model gemm_quant.rs, dense_gemv_batchm (the contract: one weight sweep for M <= 8 rows,
- * refusal of any other M); inferencelayer kernel_lab.rs, GEMV_F16S with KC columns per workgroup.
+ * Source: spark_model gemm_quant.rs, dense_gemv_batchm (the contract: one weight sweep for all M rows,
+ * refusal of any M above the compiled maximum, which the page raises from 8 to 16 with every row bit-identical
+ * to a single call); inferencelayer kernel_lab.rs, GEMV_F16S with KC columns per workgroup.
  *   Y float[M][N] (row-major), X float[M][K] (row-major, 16-byte aligned); other arguments as q4_gemv.
- *   1 <= M <= 8. Row m of Y equals q4_gemv on X[m] up to fp32 summation order.
+ *   1 <= M <= 16. Row m of Y equals q4_gemv on X[m] bit for bit (same per-row summation order and reduction
+ *   tree for every M). The M staged input vectors (M*K*4 bytes) must fit in one CTA's shared memory beside the
+ *   weight rings: all M <= 8 up to K = 4096 and M = 16 up to K = 2048; larger inputs return Q4_EUNSUPPORTED.
  */
 int q4_gemv_batched(float *Y, const uint8_t *qs, const uint16_t *d, const float *X, int M, int N, int K,
                     q4_stream_t stream);

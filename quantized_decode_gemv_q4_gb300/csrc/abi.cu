@@ -144,7 +144,7 @@ int q4_gemv_batched(float* Y, const uint8_t* qs, const uint16_t* d, const float*
     Q4_TRY(check_out(what, Y));
     Q4_TRY(check_q4_weights(what, qs, d, N, K));
     Q4_TRY(check_vec(what, "X", X));
-    if (M < 1 || M > 8) return fail(Q4_EINVAL, "%s: M=%d outside 1..8 (refused, not clamped)", what, M);
+    if (M < 1 || M > 16) return fail(Q4_EINVAL, "%s: M=%d outside 1..16 (refused, not clamped)", what, M);
     DeviceInfo di;
     Q4_TRY(check_device(what, &di));
     return finish(what, launch_q4_gemv(Y, qs, d, X, M, N, K, (cudaStream_t)stream));

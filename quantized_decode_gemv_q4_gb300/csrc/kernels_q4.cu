@@ -60,6 +60,7 @@ cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const
     if (V == 1) return dense::gemv_v1(di, Y, qs, d, X, N, K, s);
     if (V >= 2 && V <= 4) return dense::gemv_v2_4(di, Y, qs, d, X, V, N, K, s);
     if (V >= 5 && V <= 8) return dense::gemv_v5_8(di, Y, qs, d, X, V, N, K, s);
+    if (V >= 9 && V <= 16) return dense::gemv_v9_16(di, Y, qs, d, X, V, N, K, s);
     return cudaErrorInvalidValue;
 }
 

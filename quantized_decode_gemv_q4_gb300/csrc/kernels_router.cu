@@ -4,11 +4,11 @@
 // indices of the K largest logits and their softmax weights (optionally renormalised over the K). Here Wgate is
 // planar Q4 (E rows of K weights, the library's format) and x is fp32; one token per CTA row of the grid.
 //
-// Kernel shape (one CTA of W warps per token; the router matrix is small and stays in L2 after the first CTA):
+// Kernel shape (one CTA of 32 warps per token; the router matrix is small and stays in L2 after the first CTA):
 //  * stage the token's x block by block with the bias-free decode's per-block scaling (device_common.cuh);
-//  * warp w computes the logits of experts w, w + W, ...: lane l takes units l, l + 32, ... of the row with
-//    16-byte loads, one shift + eight ANDs per word and packed fp32x2 FMAs, folds each block with its scale,
-//    and the warp sums the lanes; logits go to shared memory;
+//  * warp w computes the logits of experts w, w + W, ... two rows at a time: lane l takes units l, l + 32, ...
+//    with 16-byte loads (four issued before use), one shift + eight ANDs per word and packed fp32x2 FMAs, folds
+//    each block with its scale, and the warp sums the lanes; logits go to shared memory;
 //  * warp 0 takes the softmax over all E logits (max subtracted) and K arg-max passes (ties to the lower
 //    index), writes ids and weights (and, when asked, the logits).
 #include <algorithm>
@@ -76,33 +76,60 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
     }
     __syncthreads();
 
-    // logits
-    for (int e = warp; e < p.E; e += W) {
-        float tot = 0.f;
-        for (int u = lane; u < p.nblk; u += 32) {
-            const size_t blk = (size_t)e * p.nblk + u;
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.qs) + blk);
-            const float dsc = f16_bits_to_f32(__ldg(p.d + blk));
-            const uint32_t xa = xs + xs_chunk_offset(0u, 0u, (uint32_t)u, 1u);
-            float2 acc = make_float2(0.f, 0.f);
+    // logits: warp w takes experts w and w + W, then w + 2W and w + 3W, ...; lane l units l and l + 32, then
+    // l + 64 and l + 96, ...; the four (row, unit) loads of a step are issued before any is used
+    for (int e0 = warp; e0 < p.E; e0 += 2 * W) {
+        const int ea = e0, eb = e0 + W;
+        const bool hb = eb < p.E;
+        float ta = 0.f, tb = 0.f;
+        for (int u0 = lane; u0 < p.nblk; u0 += 64) {
+            const int u1 = u0 + 32;
+            const bool h1 = u1 < p.nblk;
+            uint4 w[4];
+            uint32_t db[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const Word8s d8 = decode_word_sub(i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w);
-                const float4 xl = lds128f(xa + (uint32_t)i * 512u);
-                const float4 xh = lds128f(xa + (uint32_t)(4 + i) * 512u);
-                acc = ffma2(d8.lo01, make_float2(xl.x, xl.y), acc);
-                acc = ffma2(d8.lo23, make_float2(xl.z, xl.w), acc);
-                acc = ffma2(d8.hi01, make_float2(xh.x, xh.y), acc);
-                acc = ffma2(d8.hi23, make_float2(xh.z, xh.w), acc);
+            for (int j = 0; j < 4; ++j) {
+                const int e = (j & 2) ? eb : ea;
+                const int u = (j & 1) ? u1 : u0;
+                const bool in = ((j & 2) ? hb : true) && ((j & 1) ? h1 : true);
+                const size_t blk = (size_t)e * p.nblk + u;
+                w[j] = in ? __ldg(reinterpret_cast<const uint4*>(p.qs) + blk) : make_uint4(0u, 0u, 0u, 0u);
+                db[j] = in ? (uint32_t)__ldg(p.d + blk) : 0u;
             }
-            const float2 fa = lds64f(aux + aux_offset(0u, (uint32_t)u, 1u));
-            tot = fmaf(dsc, fmaf(acc.x + acc.y, fa.x, fa.y), tot);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int u = (j & 1) ? u1 : u0;
+                if ((j & 1) && !h1) continue;
+                const uint32_t xa = xs + xs_chunk_offset(0u, 0u, (uint32_t)u, 1u);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const Word8s d8 = decode_word_sub(i == 0 ? w[j].x : i == 1 ? w[j].y : i == 2 ? w[j].z : w[j].w);
+                    const float4 xl = lds128f(xa + (uint32_t)i * 512u);
+                    const float4 xh = lds128f(xa + (uint32_t)(4 + i) * 512u);
+                    acc = ffma2(d8.lo01, make_float2(xl.x, xl.y), acc);
+                    acc = ffma2(d8.lo23, make_float2(xl.z, xl.w), acc);
+                    acc = ffma2(d8.hi01, make_float2(xh.x, xh.y), acc);
+                    acc = ffma2(d8.hi23, make_float2(xh.z, xh.w), acc);
+                }
+                const float2 fa = lds64f(aux + aux_offset(0u, (uint32_t)u, 1u));
+                const float v = f16_bits_to_f32(db[j]) * fmaf(acc.x + acc.y, fa.x, fa.y);
+                if (j & 2) tb += v;
+                else ta += v;
+            }
         }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        for (int off = 16; off >= 1; off >>= 1) {
+            ta += __shfl_xor_sync(0xffffffffu, ta, off);
+            tb += __shfl_xor_sync(0xffffffffu, tb, off);
+        }
         if (lane == 0) {
-            if (p.logits) p.logits[(size_t)t * p.E + e] = tot;
-            lg[e] = tot != tot ? -INFINITY : tot;  // a NaN logit ranks last
+            if (p.logits) p.logits[(size_t)t * p.E + ea] = ta;
+            lg[ea] = ta != ta ? -INFINITY : ta;  // a NaN logit ranks last
+            if (hb) {
+                if (p.logits) p.logits[(size_t)t * p.E + eb] = tb;
+                lg[eb] = tb != tb ? -INFINITY : tb;
+            }
         }
     }
     __syncthreads();
@@ -171,7 +198,7 @@ cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
-    constexpr int W = 8;
+    constexpr int W = 32;
     RouterParams p;
     p.ids = ids;
     p.weights = weights;

@@ -38,7 +38,7 @@ cudaError_t launch_kernel(Kernel kern, int grid, int block, uint32_t smem, cudaS
 }
 
 // ---- planar Q4 (32-weight blocks, f16 scale per block) -------------------------------------------
-// Y[v][n] = sum_k W[n][k] * X[v][k] for v < V; V in 1..8. Returns cudaErrorNotSupported when the
+// Y[v][n] = sum_k W[n][k] * X[v][k] for v < V; V in 1..16. Returns cudaErrorNotSupported when the
 // staged input does not fit in shared memory.
 cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V, int N, int K,
                            cudaStream_t s);

@@ -1,4 +1,4 @@
-// Planar Q4 decode GEMV kernel template (sm_103a): single vector, small batch (V <= 8 vectors sharing one
+// Planar Q4 decode GEMV kernel template (sm_103a): single vector, small batch (V <= 16 vectors sharing one
 // sweep over the weights) and the pure-read ceiling instrument. Included by the kernels_q4*.cu translation
 // units, which instantiate disjoint sets of batch widths so that they compile in parallel.
 //
@@ -431,6 +431,8 @@ cudaError_t gemv_v2_4(const DeviceInfo& di, float* Y, const uint8_t* qs, const u
                       int N, int K, cudaStream_t s);
 cudaError_t gemv_v5_8(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
                       int N, int K, cudaStream_t s);
+cudaError_t gemv_v9_16(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
+                       int N, int K, cudaStream_t s);
 
 }  // namespace dense
 }  // namespace q4

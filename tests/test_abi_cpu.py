@@ -61,10 +61,10 @@ def test_refusals_need_no_gpu(lib):
     # misaligned quants and input
     assert lib.q4_gemv(P(ALIGNED), P(ALIGNED + 4), P(ALIGNED), P(ALIGNED), 4, 64, None) == q4.Q4_EALIGN
     assert lib.q4_gemv(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED + 8), 4, 64, None) == q4.Q4_EALIGN
-    # batched M outside 1..8 is refused, not clamped
-    for M in (0, 9, -1):
+    # batched M outside 1..16 is refused, not clamped
+    for M in (0, 17, -1):
         assert lib.q4_gemv_batched(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), M, 4, 64, None) == q4.Q4_EINVAL
-    assert b"M=9 outside 1..8" in (lib.q4_gemv_batched(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 9, 4, 64, None)
+    assert b"M=17 outside 1..16" in (lib.q4_gemv_batched(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 17, 4, 64, None)
                                    and lib.q4_last_error())
     # Q4_K: K must be a multiple of 256, eps finite and >= 0
     assert lib.fused_rmsnorm_q4k_gemv(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), ctypes.c_float(1e-5), 4, 128,

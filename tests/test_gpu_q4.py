@@ -56,6 +56,27 @@ def test_q4_gemv_batched_every_M(M, oracle_lib):
     assert_close(run_q4(inp, M), ref, bound, f"batched M={M}")
 
 
+@pytest.mark.parametrize("M", [9, 12, 16])
+def test_q4_gemv_batched_wide_M(M, oracle_lib):
+    """Batches of 9..16 vectors (staged input up to 16 x 2048 fp32), ragged N, and bit-identity of every row
+    with the single-vector call."""
+    inp = synth.make_q4_gemv(seed=200 + M, N=3003, K=2048, M=M)
+    ref, bound = oracle_lib.q4_gemv_batched(inp["qs"], inp["d"], inp["x"])
+    Y = run_q4(inp, M)
+    assert_close(Y, ref, bound, f"batched M={M}")
+    for t in (0, M // 2, M - 1):
+        one = dict(inp, x=inp["x"][t:t + 1])
+        assert np.array_equal(run_q4(one).view(np.uint32), Y[t].view(np.uint32)), f"row {t}"
+
+
+def test_q4_gemv_batched_wide_M_too_large_is_refused():
+    qs, d = synth.q4_weights(np.random.default_rng(2), 64, 4096)
+    X = torch.zeros(16, 4096, device="cuda")
+    Y = torch.empty(16, 64, device="cuda")
+    with pytest.raises(q4.Q4Error, match="EUNSUPPORTED"):
+        q4.q4_gemv_batched(Y, cu(qs), cu(d), X)
+
+
 @pytest.mark.parametrize("M", [2, 4, 8])
 def test_batched_rows_are_bit_identical_to_single_calls(M):
     """Row t of the batched call equals the single-vector call on x_t, bit for bit: each row keeps its own
@@ -119,9 +140,9 @@ def test_q4_dequant_is_bit_exact(N, K, oracle_lib):
 
 def test_refusals_on_device():
     qs, d = synth.q4_weights(np.random.default_rng(1), 8, 64)
-    X = torch.zeros(9, 64, device="cuda")
-    Y = torch.empty(9, 8, device="cuda")
-    with pytest.raises(q4.Q4Error, match="outside 1..8"):
+    X = torch.zeros(17, 64, device="cuda")
+    Y = torch.empty(17, 8, device="cuda")
+    with pytest.raises(q4.Q4Error, match="outside 1..16"):
         q4.q4_gemv_batched(Y, cu(qs), cu(d), X)
 
 

@@ -104,6 +104,17 @@ int fused_rmsnorm_q4k_gemv(float *y, const uint8_t *w, const float *x, const flo
                            int K, q4_stream_t stream);
 
 /*
+ * Unfused Q4_K GEMV for M input rows: Y[m][n] = sum_k W[n][k] * X[m][k] for m < M, reading every weight byte
+ * once for all M rows (no normalisation; M = 1 is the plain Q4_K GEMV).
+ * Source: trueno-gpu fused.rs (the Q4_K format of FusedRmsNormQ4KGemvKernel phase 3; the page also names an
+ * unfused Q4KGemvKernel); the batched contract of spark_model gemm_quant.rs, dense_gemv_batchm.
+ *   Y float[M][N] (row-major), X float[M][K] (row-major, 16-byte aligned), w as fused_rmsnorm_q4k_gemv.
+ *   1 <= M <= 8; N >= 1; K % 256 == 0. The M staged rows must fit in one CTA's shared memory beside the weight
+ *   rings (M*K*4 + M*K/4 bytes: M = 8 up to K = 4096); larger inputs return Q4_EUNSUPPORTED.
+ */
+int q4k_gemv_batched(float *Y, const uint8_t *w, const float *X, int M, int N, int K, q4_stream_t stream);
+
+/*
  * y_gate[n] = sum_k Wg[n][k] * xhat[k] and y_up[n] = sum_k Wu[n][k] * xhat[k] from one staged input.
  * gamma != NULL: xhat is the RMSNorm of x as in fused_rmsnorm_q4k_gemv; gamma == NULL: xhat = x.
  * Source: trueno-gpu fused.rs, FusedGateUpQ4KGemvKernel (with the full Q4_K decode for both projections).

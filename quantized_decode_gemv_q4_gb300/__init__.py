@@ -22,7 +22,7 @@ from . import build as _build
 
 __all__ = [
     "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
-    "moe_q4_gemv", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "moe_router_q4", "q4_pure_read",
+    "moe_q4_gemv", "q4k_gemv_batched", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "moe_router_q4", "q4_pure_read",
     "q4k_pure_read",
     "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
     "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "FAULT_BAD_EXPERT",
@@ -57,6 +57,7 @@ _SIGNATURES = {
     "fused_gateup_swiglu_q4k_gemv": [_P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _P],
     "moe_q4_swiglu_gemv": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
     "moe_router_q4": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "q4k_gemv_batched": [_P, _P, _P, _I, _I, _I, _P],
     "q4_device_faults": [ctypes.POINTER(ctypes.c_uint)],
 }
 
@@ -150,6 +151,16 @@ def fused_rmsnorm_q4k_gemv(y, w, x, gamma, eps: float = 1e-5, stream=None) -> No
     _check(load().fused_rmsnorm_q4k_gemv(_ptr(y, torch.float32, "y"), _ptr(w, torch.uint8, "w"),
                                          _ptr(x, torch.float32, "x"), _ptr(gamma, torch.float32, "gamma"),
                                          float(eps), N, K, _stream(stream)))
+
+
+def q4k_gemv_batched(Y, w, X, stream=None) -> None:
+    """Y[m] = W X[m] for the M rows of X (Q4_K weights, no normalisation), one weight sweep."""
+    N, K = _q4k_dims(w)
+    M = X.numel() // K
+    if X.numel() != M * K or Y.numel() != M * N:
+        raise ValueError("X must be [M, K] and Y [M, N]")
+    _check(load().q4k_gemv_batched(_ptr(Y, torch.float32, "Y"), _ptr(w, torch.uint8, "w"), _ptr(X, torch.float32, "X"),
+                                   M, N, K, _stream(stream)))
 
 
 def fused_gateup_q4k_gemv(y_gate, y_up, w_gate, w_up, x, gamma=None, eps: float = 1e-5, stream=None) -> None:

@@ -163,6 +163,17 @@ int fused_rmsnorm_q4k_gemv(float* y, const uint8_t* w, const float* x, const flo
     return finish(what, launch_q4k_gemv(y, nullptr, w, nullptr, x, gamma, eps, N, K, false, (cudaStream_t)stream));
 }
 
+int q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, int M, int N, int K, q4_stream_t stream) {
+    const char* what = "q4k_gemv_batched";
+    Q4_TRY(check_out(what, Y));
+    Q4_TRY(check_q4k_weights(what, w, N, K));
+    Q4_TRY(check_vec(what, "X", X));
+    if (M < 1 || M > 8) return fail(Q4_EINVAL, "%s: M=%d outside 1..8 (refused, not clamped)", what, M);
+    DeviceInfo di;
+    Q4_TRY(check_device(what, &di));
+    return finish(what, launch_q4k_gemv_batched(Y, w, X, M, N, K, (cudaStream_t)stream));
+}
+
 int fused_gateup_q4k_gemv(float* y_gate, float* y_up, const uint8_t* w_gate, const uint8_t* w_up, const float* x,
                           const float* gamma, float eps, int N, int K, q4_stream_t stream) {
     const char* what = "fused_gateup_q4k_gemv";

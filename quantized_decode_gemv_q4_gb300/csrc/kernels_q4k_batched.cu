@@ -1,0 +1,322 @@
+// Batched (unfused) Q4_K decode GEMV for sm_103a: Y[v][n] = sum_k W[n][k] * X[v][k] for v < V <= 8, reading
+// every weight byte once for all V vectors.
+//
+// Format: trueno-gpu `fused.rs`, FusedRmsNormQ4KGemvKernel phase 3 (144-byte super-blocks of 256 weights;
+// value d*sc_j*q - dmin*m_j); the page also names an unfused Q4KGemvKernel. Batched contract as the planar
+// form (spark_model `gemm_quant.rs`, dense_gemv_batchm: one sweep for all rows).
+//
+// Kernel shape (one persistent CTA of W warps per SM), the Q4_K kernel's with V vectors:
+//  * the V vectors are staged once per CTA, each 32-element sub-block with its own exponent bound e_{j,v}
+//    (bias-free decode, device_common.cuh), beside (S_{j,v}, 2^(22+e_{j,v}));
+//  * each warp streams R rows (whole rows when they fit) through its own ring of cp.async slots;
+//  * lane l takes unit l (+32, ...) of every row: chunk c = (l%8)/2, half l%2; the 8 lanes of a super-block
+//    each decode one sub-block's header entry (d*sc_j and dmin*m_j), shared with the group by shuffles;
+//  * per word: one shift + eight ANDs per row, then for each vector two staged-input loads (shared by the R
+//    rows) and four packed FMAs per row into one accumulator per sub-block; per unit and vector the two
+//    accumulators fold with d*sc*2^(22+e) of their sub-block, and each lane adds dmin*m_j*S_{j,v} of its own
+//    sub-block (the warp reduction sums the eight);
+//  * the R*V totals are summed over the warp with the transposing shuffle reduction and stored.
+#include <algorithm>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace q4 {
+
+namespace {
+
+struct Q4KBParams {
+    float* y;
+    const uint8_t* w;
+    const float* x;
+    int N, K, nsb;
+    int CS, S, jobs, slot_bytes;
+    uint32_t xs_off, ssum_off, slots_off;
+};
+
+__device__ __forceinline__ float byte_as_float_b(uint32_t w, int j) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + (uint32_t)j)) - 8388608.0f;
+}
+
+template <int V, int R, int W, int D>
+__global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams p) {
+    constexpr int kThreads = W * 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t U = (uint32_t)(p.K / 32);
+    const int nsub = p.K / 32;
+
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t xs = s_base + p.xs_off;      // float[V][8 quads][U][4]
+    const uint32_t ssum = s_base + p.ssum_off;  // float2[V][K/32]: (S_j, 2^(22+e_j))
+    const uint32_t ring = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
+
+    const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
+    const int Wtot = (int)gridDim.x * W;
+    const uint64_t pol = policy_evict_first();
+    const size_t row_bytes = (size_t)p.nsb * 144;
+
+    int ijob = gw, ic = 0, islot = 0;
+    auto issue = [&]() {
+        if (ijob < p.jobs) {
+            const int r0 = ijob * R;
+            const int rv = min(R, p.N - r0);
+            const int sb0 = ic * p.CS;
+            const int cs = min(p.CS, p.nsb - sb0);
+            const uint32_t slot = ring + (uint32_t)(islot * p.slot_bytes);
+            const uint8_t* src = p.w + (size_t)r0 * row_bytes + (size_t)sb0 * 144;
+            if (p.S == 1) {
+                warp_copy_async(slot, src, (uint32_t)(rv * cs * 144), lane, pol);
+            } else {
+                for (int r = 0; r < rv; ++r)
+                    warp_copy_async(slot + (uint32_t)(r * cs * 144), src + (size_t)r * row_bytes, (uint32_t)(cs * 144),
+                                    lane, pol);
+            }
+            if (++ic == p.S) {
+                ic = 0;
+                ijob += Wtot;
+            }
+            islot = islot + 1 == D ? 0 : islot + 1;
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue();
+
+    // The weights are constant; X and Y may belong to the previous kernel in the stream.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // Stage the V vectors: four lanes per sub-block (whole warps: V*K/32*4 is a multiple of 32).
+    {
+        const int t4 = lane & 3;
+        for (int thr = threadIdx.x; thr < V * nsub * 4; thr += kThreads) {
+            const int jsv = thr >> 2;  // v * nsub + js
+            const int v = jsv / nsub;
+            const int js = jsv - v * nsub;
+            const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)jsv * 8 + 2 * t4;
+            const int k = js & 1;
+            const Stage4 st = stage_block4(__ldg(src), __ldg(src + 1), k);
+            const uint32_t u = (uint32_t)(js & ~1) + (uint32_t)(t4 >> 1);
+            const uint32_t q0 = (uint32_t)(4 * k + ((2 * t4) & 3));
+            const uint32_t a0 = xs + xs_index((uint32_t)v, q0, u, U) * 4u;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y), "f"(st.a.z),
+                         "f"(st.a.w)
+                         : "memory");
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + U * 16u), "f"(st.b.x), "f"(st.b.y),
+                         "f"(st.b.z), "f"(st.b.w)
+                         : "memory");
+            if (t4 == 0)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ssum + (uint32_t)jsv * 8u), "f"(st.sum),
+                             "f"(block_factor(st.e))
+                             : "memory");
+        }
+    }
+    __syncthreads();
+
+    float2 tot[R][V];
+    float mins[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            tot[r][v] = make_float2(0.f, 0.f);
+            mins[r][v] = 0.f;
+        }
+
+    const uint32_t cpos = (uint32_t)(lane & 7);
+    const uint32_t jj = cpos & 3u;
+    const int gbase = lane & ~7;
+    const uint32_t qstride = U * 16u;
+    const uint32_t vstride = 8u * U * 16u;
+    const int my_jobs = gw < p.jobs ? (p.jobs - 1 - gw) / Wtot + 1 : 0;
+    const int total = my_jobs * p.S;
+    int job = gw, c = 0, cslot = 0;
+    for (int g = 0; g < total; ++g) {
+        issue();
+        cp_async_wait<D - 1>();
+        __syncwarp();
+        const uint32_t slot = ring + (uint32_t)(cslot * p.slot_bytes);
+        const int r0 = job * R;
+        const int rv = min(R, p.N - r0);
+        const int sb0 = c * p.CS;
+        const int cs = min(p.CS, p.nsb - sb0);
+        const int nunits = 8 * cs;
+
+        // Uniform trip count over the warp (lanes past the chunk use a clamped super-block and add nothing),
+        // so every lane takes part in the shuffles.
+#pragma unroll 1
+        for (int ul0 = 0; ul0 < nunits; ul0 += 32) {
+            const int ul = ul0 + lane;
+            const bool valid = ul < nunits;
+            const int sbl = valid ? (ul >> 3) : 0;
+            const uint32_t u = (uint32_t)(8 * (sb0 + sbl)) + cpos;  // unit index = sub-block index of j = cpos
+            uint4 w[R];
+            float dlo[R], dhi[R], dmm[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t it = (uint32_t)(r * cs + sbl);
+                const uint4 hdr = lds128(slot + it * 144u);
+                const uint32_t scw = cpos < 4 ? (hdr.y & 0x3F3F3F3Fu)
+                                              : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+                const uint32_t mw = cpos < 4 ? (hdr.z & 0x3F3F3F3Fu)
+                                             : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+                const float dsc = f16_bits_to_f32(hdr.x) * byte_as_float_b(scw, (int)jj);
+                dmm[r] = f16_bits_to_f32(hdr.x >> 16) * byte_as_float_b(mw, (int)jj);
+                dlo[r] = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos & ~1u));
+                dhi[r] = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos | 1u));
+                w[r] = lds128(slot + it * 144u + 16u + cpos * 16u);
+            }
+            float2 aL[R][V], aH[R][V];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Word8s d8[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const uint32_t xa = xs + (uint32_t)v * vstride + u * 16u;
+                    const float4 xl = lds128f(xa + (uint32_t)i * qstride);
+                    const float4 xh = lds128f(xa + (uint32_t)(4 + i) * qstride);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        float2 a = i == 0 ? make_float2(0.f, 0.f) : aL[r][v];
+                        float2 b = i == 0 ? make_float2(0.f, 0.f) : aH[r][v];
+                        a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
+                        a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
+                        b = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), b);
+                        b = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), b);
+                        aL[r][v] = a;
+                        aH[r][v] = b;
+                    }
+                }
+            }
+            if (valid) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    // (S, f) of sub-blocks 2c and 2c+1 of this super-block for vector v
+                    const float4 sf = lds128f(ssum + ((uint32_t)v * (uint32_t)nsub + (u & ~1u)) * 8u);
+                    const float s_own = (cpos & 1u) ? sf.z : sf.x;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float fl = dlo[r] * sf.y;
+                        const float fh = dhi[r] * sf.w;
+                        tot[r][v] = ffma2(make_float2(fl, fl), aL[r][v], tot[r][v]);
+                        tot[r][v] = ffma2(make_float2(fh, fh), aH[r][v], tot[r][v]);
+                        mins[r][v] = fmaf(dmm[r], s_own, mins[r][v]);
+                    }
+                }
+            }
+        }
+        __syncwarp();  // every lane is done with this slot before a later stage reuses it
+
+        if (c == p.S - 1) {
+            constexpr int NV = R * V;
+            constexpr int P2 = NextPow2<NV>::value;
+            constexpr int L2 = log2_const<P2>();
+            float vals[P2];
+#pragma unroll
+            for (int i = 0; i < P2; ++i) vals[i] = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    vals[r * V + v] = (tot[r][v].x + tot[r][v].y) - mins[r][v];
+                    tot[r][v] = make_float2(0.f, 0.f);
+                    mins[r][v] = 0.f;
+                }
+            warp_transpose_reduce<P2>(vals, lane);
+            const int idx = lane >> (5 - L2);
+            const bool leader = (lane & ((1 << (5 - L2)) - 1)) == 0;
+            if (leader && idx < NV) {
+                const int r = idx / V;
+                const int v = idx - r * V;
+                if (r < rv) p.y[(size_t)v * p.N + r0 + r] = vals[0];
+            }
+        }
+        if (++c == p.S) {
+            c = 0;
+            job += Wtot;
+        }
+        cslot = cslot + 1 == D ? 0 : cslot + 1;
+    }
+}
+
+inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Shared memory: [staged X V*K*4][(S, factor) V*K/32*8][W rings of D slots of R rows x CS super-blocks];
+// whole rows first, then smaller chunks, then depth 2.
+template <int V, int R, int W>
+cudaError_t run_batched(const DeviceInfo& di, float* Y, const uint8_t* w, const float* X, int N, int K,
+                        cudaStream_t s) {
+    const int nsb = K / 256;
+    Q4KBParams p;
+    p.y = Y;
+    p.w = w;
+    p.x = X;
+    p.N = N;
+    p.K = K;
+    p.nsb = nsb;
+    const uint32_t xsb = (uint32_t)round_up(V * K * 4, 128);
+    const uint32_t ssb = (uint32_t)round_up(V * (K / 32) * 8, 128);
+    p.xs_off = 0;
+    p.ssum_off = xsb;
+    p.slots_off = xsb + ssb;
+    for (int dd = 3; dd >= 2; --dd) {
+        for (int cs0 = 16; cs0 >= 1; cs0 /= 2) {
+            const int cs = std::min(cs0, nsb);
+            const int slot = round_up(R * cs * 144, 128);
+            const uint32_t smem = p.slots_off + (uint32_t)(W * dd * slot);
+            if (smem > (uint32_t)di.max_smem_optin) continue;
+            p.CS = cs;
+            p.S = (nsb + cs - 1) / cs;
+            p.jobs = (N + R - 1) / R;
+            p.slot_bytes = slot;
+            const int grid = std::min(di.sm_count, p.jobs);
+            cudaError_t err = cudaSuccess;
+            if (dd == 3) {
+                auto kern = q4k_batched_kernel<V, R, W, 3>;
+                static std::once_flag once3[64];
+                std::call_once(once3[di.device & 63], [&] {
+                    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+                });
+                if (err != cudaSuccess) return err;
+                return launch_kernel(kern, grid, W * 32, smem, s, p);
+            }
+            auto kern = q4k_batched_kernel<V, R, W, 2>;
+            static std::once_flag once2[64];
+            std::call_once(once2[di.device & 63], [&] {
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+            });
+            if (err != cudaSuccess) return err;
+            return launch_kernel(kern, grid, W * 32, smem, s, p);
+        }
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+// Variant per batch width: 16 warps x 2 rows for one or two vectors, 8 warps x 2 rows above.
+cudaError_t launch_q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, int V, int N, int K, cudaStream_t s) {
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess) return e;
+    switch (V) {
+        case 1: return run_batched<1, 2, 16>(di, Y, w, X, N, K, s);
+        case 2: return run_batched<2, 2, 16>(di, Y, w, X, N, K, s);
+        case 3: return run_batched<3, 2, 8>(di, Y, w, X, N, K, s);
+        case 4: return run_batched<4, 2, 8>(di, Y, w, X, N, K, s);
+        case 5: return run_batched<5, 2, 8>(di, Y, w, X, N, K, s);
+        case 6: return run_batched<6, 2, 8>(di, Y, w, X, N, K, s);
+        case 7: return run_batched<7, 2, 8>(di, Y, w, X, N, K, s);
+        case 8: return run_batched<8, 2, 8>(di, Y, w, X, N, K, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace q4

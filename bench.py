@@ -524,6 +524,26 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
                     for s in range(replicas)], stream)
     out[f"moe_q4_swiglu_gemv e64 1408x2048 t8k8 ({uniq} experts)"] = {
         "us": round(us, 3), "weight_GBps": round(mb / us / 1e3, 1), "frac_of_hbm_peak": round(mb / us / 1e3 / peak, 4)}
+    # unfused batched Q4_K on the gate matrix of the gate+up workload, and the planar batched GEMV at M = 16
+    kb = q4k_bytes(18944, 3584)
+    Xk = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 8, 3584))).to(dev)
+    for M in (1, 8):
+        Yk = torch.empty(M, 18944, device=dev)
+        mats = [suite.sets[s]["c3"][j] for s in range(replicas) for j in (0, 1)]  # 4 x 38 MB rotated
+        us = _graph_us([lambda m=m: q4.q4k_gemv_batched(Yk, m, Xk[:M]) for m in mats], stream)
+        out[f"q4k_gemv_batched 18944x3584 M={M}"] = {"us": round(us, 3), "weight_GBps": round(kb / us / 1e3, 1),
+                                                     "frac_of_hbm_peak": round(kb / us / 1e3 / peak, 4)}
+    qs16, d16 = synth.q4_weights(rng, 14336, 2048)
+    b16 = q4_bytes(14336, 2048)
+    n16 = int(np.ceil(3 * L2_BYTES / b16))  # copies rotated so every call reads cold weights (3x the L2)
+    w16 = [(cu(qs16), cu(d16)) for _ in range(n16)]
+    X16 = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 16, 2048))).to(dev)
+    Y16 = torch.empty(16, 14336, device=dev)
+    us = _graph_us([lambda i=i: q4.q4_gemv_batched(Y16, w16[i][0], w16[i][1], X16) for i in range(n16)], stream,
+                   reps=n16)
+    out["q4_gemv_batched 14336x2048 M=16"] = {"us": round(us, 3), "weight_GBps": round(b16 / us / 1e3, 1),
+                                              "fp32_TFLOPs": round(16 * 2 * 14336 * 2048 / us / 1e6, 2)}
+    del w16
     # dependent chain: the router's ids drive the MoE call on the device
     chain = []
     for ov in (True, False):

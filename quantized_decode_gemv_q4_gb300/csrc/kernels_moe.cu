@@ -37,7 +37,7 @@ static __device__ unsigned g_fault_moe;
 
 namespace {
 
-constexpr int kMaxSlots = 512;  // T * topk
+constexpr int kMaxSlots = 512;  // largest T * topk
 constexpr int kMaxC = 4;        // routed slots served per weight sweep
 
 struct MoEParams {
@@ -52,17 +52,19 @@ struct MoEParams {
     int32_t* status;
     int T, topk, E, N, K, nblk;
     int S, dcopy;
+    int ms;    // routing table stride: T*topk rounded up to 32
+    int deal;  // 1: jobs dealt round-robin over the warps; 0: contiguous cost-balanced ranges
     int cost_a, cost_b;
     uint32_t route_off, xs_off, aux_off, slots_off;
     unsigned* fault;
 };
 
-// Routing tables in shared memory (route_off): slot_ids[kMaxSlots], rank[kMaxSlots], owner[kMaxSlots],
-// ucount[kMaxSlots], uoffset[kMaxSlots+1], list[kMaxSlots], group_ux[kMaxSlots], group_first[kMaxSlots],
-// group_cnt[kMaxSlots], scalars[4] (number of distinct experts, number of groups), then the cumulative job
-// cost gcum[kMaxSlots+1] (64-bit) and the job order of the groups gorder[kMaxSlots] (groups sorted by slot
+// Routing tables in shared memory (route_off), each of ms = T*topk rounded up to 32 entries: slot_ids, rank,
+// owner, ucount, uoffset (ms+1), list, group_ux, group_first, group_cnt, scalars[4] (number of distinct experts,
+// number of groups), then the cumulative job cost gcum[ms+1] (64-bit) and the job order of the groups gorder
+// (groups sorted by slot
 // count).
-constexpr int kRouteInts = 9 * kMaxSlots + 8 + 2 * (kMaxSlots + 1) + 2 + kMaxSlots;
+__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + ms; }
 
 // Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
 // (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
@@ -98,17 +100,18 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 
     int* route = reinterpret_cast<int*>(smem + p.route_off);
     int* slot_ids = route;
-    int* rank = route + kMaxSlots;
-    int* owner = route + 2 * kMaxSlots;
-    int* ucount = route + 3 * kMaxSlots;
-    int* uoffset = route + 4 * kMaxSlots;  // kMaxSlots + 1 entries
-    int* list = route + 5 * kMaxSlots + 1;
-    int* group_ux = route + 6 * kMaxSlots + 1;
-    int* group_first = route + 7 * kMaxSlots + 1;
-    int* group_cnt = route + 8 * kMaxSlots + 1;
-    int* scalars = route + 9 * kMaxSlots + 1;
-    long long* gcum = reinterpret_cast<long long*>(route + 9 * kMaxSlots + 8);  // 8-byte aligned
-    int* gorder = route + 9 * kMaxSlots + 8 + 2 * (kMaxSlots + 1) + 2;
+    const int ms = p.ms;
+    int* rank = route + ms;
+    int* owner = route + 2 * ms;
+    int* ucount = route + 3 * ms;
+    int* uoffset = route + 4 * ms;  // ms + 1 entries
+    int* list = route + 5 * ms + 1;
+    int* group_ux = route + 6 * ms + 1;
+    int* group_first = route + 7 * ms + 1;
+    int* group_cnt = route + 8 * ms + 1;
+    int* scalars = route + 9 * ms + 1;
+    long long* gcum = reinterpret_cast<long long*>(route + 9 * ms + 8);  // 8-byte aligned (ms % 32 == 0)
+    int* gorder = route + 9 * ms + 8 + 2 * (ms + 1) + 2;
 
     // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
     // in the stream (it may have written ids, x or the outputs) before anything else.
@@ -227,9 +230,11 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
     const int jobs = ngroups * NP * rgs;
-    // Warps are numbered CTA by CTA, and the groups run in order of slot count, so the warps of one SM own
-    // neighbouring job ranges and mostly run the same compiled stage body (one set of instructions hot).
-    const int gw = (int)blockIdx.x * W + warp;
+    // Groups run in order of slot count. Round-robin dealing (p.deal = 1): warp gw (numbered across CTAs
+    // first) takes jobs gw, gw + Wtot, ..., so at any moment the grid sweeps neighbouring rows of one expert
+    // matrix and the warps of an SM run the same compiled stage body. Range dealing (p.deal = 0): warps
+    // numbered CTA by CTA own contiguous job ranges of equal estimated cost.
+    const int gw = p.deal ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * W + warp;
     const int Wtot = (int)gridDim.x * W;
     // Job order of the groups (stable by slot count), then the cumulative cost in that order (each group has
     // 2 * rgs jobs of cost job_cost(cnt)), then this warp's share of the total cost as a contiguous job range
@@ -272,8 +277,9 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         }
         return lo * NP * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]] & 0xFF, PURE, p.cost_a, p.cost_b));
     };
-    const int j0 = job_at(total_cost * gw / Wtot);
-    const int j1 = job_at(total_cost * (gw + 1) / Wtot);
+    const int j0 = p.deal ? gw : job_at(total_cost * gw / Wtot);
+    const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : job_at(total_cost * (gw + 1) / Wtot);
+    const int jstep = p.deal ? Wtot : 1;  // job stride of this warp
     const uint64_t pol = policy_evict_first();
 
     // Job cursor: group, projection, row group, chunk. Jobs run group-major, then projection, then row
@@ -293,8 +299,9 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     auto advance = [&](Cursor& k) {
         if (++k.c == p.S) {
             k.c = 0;
-            if (++k.rg == rgs) {
-                k.rg = 0;
+            k.rg += jstep;
+            while (k.rg >= rgs) {
+                k.rg -= rgs;
                 if (++k.sp == NP) {
                     k.sp = 0;
                     ++k.grp;
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         }
     };
 
-    const int total = (j1 - j0) * p.S;
+    const int total = (p.deal ? (j1 - j0) : (j1 - j0)) * p.S;  // jobs of this warp x chunks
     Cursor ik = cursor_at(j0);
     int issued = 0, islot = 0;
     auto issue = [&]() {
@@ -546,17 +553,18 @@ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 // Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b"
 // (variant 48: 4 rows x 8 warps; 216: 2 rows x 16 warps; job cost cost_a + cost_b * C). Used for tuning
 // sweeps; the defaults come from such sweeps.
-void plan_override(int* variant, int* depth, int* cost_a, int* cost_b) {
-    static int o_v = -1, o_d = -1, o_a = -1, o_b = -1;
+void plan_override(int* variant, int* depth, int* cost_a, int* cost_b, int* deal) {
+    static int o_v = -1, o_d = -1, o_a = -1, o_b = -1, o_deal = -1;
     static std::once_flag once;
     std::call_once(once, [] {
         const char* e = getenv("Q4GEMV_MOE_PLAN");
-        if (e) sscanf(e, "%d,%d,%d,%d", &o_v, &o_d, &o_a, &o_b);
+        if (e) sscanf(e, "%d,%d,%d,%d,%d", &o_v, &o_d, &o_a, &o_b, &o_deal);
     });
     if (o_v > 0) *variant = o_v;
     if (o_d > 0) *depth = o_d;
     if (o_a > 0) *cost_a = o_a;
     if (o_b > 0) *cost_b = o_b;
+    if (o_deal >= 0) *deal = o_deal;
 }
 
 unsigned* fault_word(int device) {
@@ -573,7 +581,7 @@ unsigned* fault_word(int device) {
 
 template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
-    const uint32_t route = (uint32_t)round_up(kRouteInts * 4, 128);
+    const uint32_t route = (uint32_t)round_up(route_ints(p.ms) * 4, 128);
     const uint32_t xsb = PURE ? 0u : (uint32_t)round_up(p.T * p.K * 4, 128);
     const uint32_t axb = PURE ? 0u : (uint32_t)round_up(p.T * p.nblk * 8, 128);
     p.route_off = 0;
@@ -639,6 +647,7 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.N = N;
     p.K = K;
     p.nblk = K / 32;
+    p.ms = (T * topk + 31) / 32 * 32;
     p.dcopy = (p.nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(d_gate) & 15u) == 0) &&
               ((reinterpret_cast<uintptr_t>(d_up) & 15u) == 0);
     p.fault = fault_word(di.device);
@@ -646,7 +655,8 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     int variant = 48, depth = 3;
     p.cost_a = 9;
     p.cost_b = 5;
-    plan_override(&variant, &depth, &p.cost_a, &p.cost_b);
+    p.deal = 1;
+    plan_override(&variant, &depth, &p.cost_a, &p.cost_b, &p.deal);
     if (pure_read) return variant == 216 ? launch<2, 16, true>(di, p, depth, s) : launch<4, 8, true>(di, p, depth, s);
     if (swiglu) {  // R gate + R up rows per slot
         if (variant == 216) return launch<1, 16, false, true>(di, p, depth, s);

@@ -24,6 +24,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <string>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -469,8 +470,21 @@ cudaError_t run(const DeviceInfo& di, const Args& a, int CS, int D, cudaStream_t
 
 }  // namespace
 
+// Developer switch to the warp-per-row-group kernels above, read once from Q4GEMV_Q4K_IMPL=warp; the
+// row-per-lane kernels are the default.
+bool use_warp_impl() {
+    static bool w = false;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* e = getenv("Q4GEMV_Q4K_IMPL");
+        w = e && std::string(e) == "warp";
+    });
+    return w;
+}
+
 cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
                             const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s) {
+    if (!use_warp_impl()) return launch_q4k_rows_gemv(y0, y1, w0, w1, x, gamma, eps, N, K, swiglu, s);
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
@@ -487,6 +501,7 @@ cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8
 }
 
 cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s) {
+    if (!use_warp_impl()) return launch_q4k_rows_pure_read(sink, w, N, K, s);
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;

@@ -51,6 +51,10 @@ cudaError_t launch_q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, in
 // y0 = silu(W0 xhat) * (W1 xhat) and y1 is not written.
 cudaError_t launch_q4k_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
                             const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s);
+// Row-per-lane forms of launch_q4k_gemv and launch_q4k_pure_read (kernels_q4k_rows.cu).
+cudaError_t launch_q4k_rows_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
+                                 const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s);
+cudaError_t launch_q4k_rows_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s);
 // Y[v][n] = sum_k W[n][k] * X[v][k], V in 1..8, no normalisation.
 cudaError_t launch_q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, int V, int N, int K, cudaStream_t s);
 cudaError_t launch_q4k_pure_read(float* sink, const uint8_t* w, int N, int K, cudaStream_t s);

@@ -164,14 +164,19 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
 
     // Register-resident input (V = 1, whole rows in one chunk): the quads and block pairs of this lane's
     // units. Quads of units past the row end are never used.
+    // Plain pointers into the shared array (not asm address operands), so that the unit offsets below fold
+    // into the loads' immediates.
+    const float4* const xs_p = reinterpret_cast<const float4*>(smem + p.xs_off) + lane;
+    const float2* const aux_p = reinterpret_cast<const float2*>(smem + p.aux_off) + lane;
+    const uint8_t* const ring_p = smem + p.slots_off + (size_t)warp * (D * SLOT);
     float4 xr[XREG ? UPL : 1][8];
     float2 ar[XREG ? UPL : 1];
     if constexpr (XREG) {
 #pragma unroll
         for (int it = 0; it < UPL; ++it) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) xr[it][q] = lds128f(xs + (uint32_t)(it * 4096 + q * 512) + (uint32_t)lane * 16u);
-            ar[it] = lds64f(aux + (uint32_t)(it * 256) + (uint32_t)lane * 8u);
+            for (int q = 0; q < 8; ++q) xr[it][q] = xs_p[it * 256 + q * 32];
+            ar[it] = aux_p[it * 32];
         }
     }
 
@@ -191,15 +196,15 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
         issue();                 // stage g + D - 1 into the slot consumed at g - 1
         cp_async_wait<D - 1>();  // stage g has landed
         __syncwarp();
-        const uint32_t slot = ring + (uint32_t)cslot * SLOT;
+        const uint8_t* const slot_p = ring_p + cslot * SLOT;
         const int r0 = job * R;
         const int rv = min(R, p.N - r0);
         const int b0 = c * CB;
         const int nb = min(CB, p.nblk - b0);
-        const uint32_t qb = slot + (uint32_t)lane * 16u;
-        const uint32_t db = slot + QBYTES + (uint32_t)lane * 2u;
-        const uint32_t xb = xs + (uint32_t)(b0 >> 5) * (uint32_t)(V * 4096) + (uint32_t)lane * 16u;
-        const uint32_t ab = aux + (uint32_t)(b0 >> 5) * (uint32_t)(V * 256) + (uint32_t)lane * 8u;
+        const uint4* const qb = reinterpret_cast<const uint4*>(slot_p) + lane;
+        const uint16_t* const db = reinterpret_cast<const uint16_t*>(slot_p + QBYTES) + lane;
+        const float4* const xb = xs_p + (b0 >> 5) * (V * 256);
+        const float2* const ab = aux_p + (b0 >> 5) * (V * 32);
 
         auto unit = [&](const int it) {
             uint4 w[R];
@@ -207,9 +212,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
             uint32_t dbits[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                w[r] = lds128(qb + (uint32_t)r * QROW + (uint32_t)(it * 512));
+                w[r] = qb[r * (QROW / 16) + it * 32];
                 if (p.dcopy)
-                    dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
+                    dbits[r] = db[r * CB + it * 32];
                 else
                     dbits[r] = r < rv ? (uint32_t)__ldg(p.d + (size_t)(r0 + r) * p.nblk + b0 + it * 32 + lane) : 0u;
                 dsc[r] = f16_bits_to_f32(dbits[r]);
@@ -234,9 +239,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                             xl = xr[it][i];
                             xh = xr[it][4 + i];
                         } else {
-                            const uint32_t xa = xb + (uint32_t)((it * V + v) * 4096 + i * 512);
-                            xl = lds128f(xa);
-                            xh = lds128f(xa + 2048u);
+                            const float4* const xa = xb + (it * V + v) * 256 + i * 32;
+                            xl = xa[0];
+                            xh = xa[128];
                         }
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                     if constexpr (XREG)
                         fa = ar[it];
                     else
-                        fa = lds64f(ab + (uint32_t)((it * V + v) * 256));
+                        fa = ab[(it * V + v) * 32];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const float2 sa = NCH == 1 ? acc[r][v][0] : fadd2(acc[r][v][0], acc[r][v][NCH - 1]);

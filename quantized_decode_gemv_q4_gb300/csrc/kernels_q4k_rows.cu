@@ -25,6 +25,8 @@
 #include <cstdlib>
 #include <mutex>
 
+#include <cuda.h>  // tensor-map types (the encoder is reached through the runtime's driver entry point)
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -36,8 +38,10 @@ constexpr int kSB = 144;                   // bytes per super-block
 constexpr int kPieces = kSB / 16;          // 16-byte copy pieces per super-block
 constexpr uint32_t kSlot = 32u * kSB;      // one stage: a super-block of each of the 32 lane rows
 constexpr int kMaxWarps = 16;
+constexpr int kGroupMax = 4;               // tiles whose partial sums meet at one CTA barrier
 
 struct RowParams {
+    CUtensorMap tm0, tm1;  // weight matrices as 2-D byte tensors [N][row bytes], box 144 x rows per stream
     float* y0;
     float* y1;
     const uint8_t* w0;
@@ -48,8 +52,11 @@ struct RowParams {
     int swiglu;          // two streams only: y0 = silu(gate) * up, y1 unused
     int N, K, nsb;
     int tiles;           // ceil(N / rows per tile)
-    uint32_t xs_off, ss_off, red_off, slots_off;
+    int nb;              // tiles per reduction group, 1..kGroupMax
+    uint32_t xs_off, ss_off, red_off, bar_off, slots_off;
 };
+
+constexpr long long kWaitCycles = 4000000000LL;  // bound on one wait for a stage (about two seconds)
 
 // byte j of w as an exact float (0x4B000000 | b is 2^23 + b)
 __device__ __forceinline__ float sbyte(uint32_t w, int j) {
@@ -61,8 +68,33 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
                  : "memory");
 }
 
-template <int NS, int D, bool PURE>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowParams p) {
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n selp.u32 %0, 1, 0, P;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+// 2-D tensor tile (x bytes in, y rows down) into shared memory, completing on the mbarrier's transaction count
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+template <int NS, int D, bool PURE, bool TMA>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __grid_constant__ RowParams p) {
     constexpr int TR = 32 / NS;  // rows per tile and stream
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -72,6 +104,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
     const uint32_t ring = smem_addr(smem) + p.slots_off + (uint32_t)(warp * D) * kSlot;
     const uint8_t* const ring_p = smem + p.slots_off + (size_t)(warp * D) * kSlot;
     const uint64_t pol = policy_evict_first();
+    const uint32_t bars = smem_addr(smem) + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot
+    // set when a stage wait ran out: the CTA's rows are then stored as NaN
+    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + kMaxWarps * 3 * 8);
+    if (threadIdx.x == 0) s_err = 0;
+    if constexpr (TMA) {
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < D; ++k) mbar_init(bars + 8u * k, 1u);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
 
     // Copy pieces of this lane: piece j*32 + lane of a stage is bytes [16k, 16k+16) of lane row
     // (j*32 + lane) / 9, which is row rr of stream 0 or 1 of the tile.
@@ -102,10 +146,26 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
             const int sb = warp + ik * nw;
             const uint8_t* b0 = p.w0 + (size_t)r0 * row_bytes + (size_t)sb * kSB;
             const uint8_t* b1 = NS == 2 ? p.w1 + (size_t)r0 * row_bytes + (size_t)sb * kSB : b0;
-            const uint32_t dst = ring + (uint32_t)islot * kSlot + (uint32_t)lane * 16u;
+            if constexpr (TMA) {
+                // one bulk tensor copy per stream by lane 0 (rows past N arrive zero-filled); this warp's
+                // earlier reads of the slot are ordered before the asynchronous write
+                if (lane == 0) {
+                    const uint32_t bar = bars + 8u * (uint32_t)islot;
+                    const uint32_t dst = ring + (uint32_t)islot * kSlot;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(bar, kSlot);
+                    tma_load_2d(dst, &p.tm0, sb * kSB, r0, bar, pol);
+                    if constexpr (NS == 2) tma_load_2d(dst + (uint32_t)(TR * kSB), &p.tm1, sb * kSB, r0, bar, pol);
+                }
+                (void)nv;
+                (void)b0;
+                (void)b1;
+            } else {
+                const uint32_t dst = ring + (uint32_t)islot * kSlot + (uint32_t)lane * 16u;
 #pragma unroll
-            for (int j = 0; j < kPieces; ++j)
-                if (prow[j] < nv) cp_async16(dst + (uint32_t)(j * 512), ((s1mask >> j) & 1u ? b1 : b0) + soff[j], pol);
+                for (int j = 0; j < kPieces; ++j)
+                    if (prow[j] < nv) cp_async16(dst + (uint32_t)(j * 512), ((s1mask >> j) & 1u ? b1 : b0) + soff[j], pol);
+            }
             ++iss;
             if (++ik == spb) {
                 ik = 0;
@@ -113,7 +173,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
             }
             islot = islot + 1 == D ? 0 : islot + 1;
         }
-        cp_async_commit();
+        if constexpr (!TMA) cp_async_commit();
     };
 
 #pragma unroll
@@ -123,7 +183,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
     grid_dependency_wait();
     grid_launch_dependents();
 
-    float* const red = reinterpret_cast<float*>(smem + p.red_off);  // [2][kMaxWarps][32] + [kMaxWarps]
+    float* const red = reinterpret_cast<float*>(smem + p.red_off);  // [2][kGroupMax][kMaxWarps][32] + [kMaxWarps]
     if constexpr (!PURE) {
         const int nthreads = (int)blockDim.x;
         float r = 1.0f;
@@ -148,7 +208,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            float* const part = red + 2 * kMaxWarps * 32;
+            float* const part = red + 2 * kGroupMax * kMaxWarps * 32;
             if (lane == 0) part[warp] = ss;
             __syncthreads();
             float tot = 0.f;
@@ -183,9 +243,24 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
     float tot = 0.f;
     uint32_t fold = 0u;
     int tile = (int)blockIdx.x, k = 0, cslot = 0, tcount = 0;
+    uint32_t cphase = 0u;
     for (int g = 0; g < total; ++g) {
-        issue();                 // stage g + D - 1 into the slot consumed at g - 1
-        cp_async_wait<D - 1>();  // stage g has landed
+        issue();  // stage g + D - 1 into the slot consumed at g - 1
+        if constexpr (TMA) {
+            // stage g has landed once its slot's mbarrier completes phase cphase; the wait is bounded
+            const uint32_t bar = bars + 8u * (uint32_t)cslot;
+            if (!mbar_try_wait(bar, cphase)) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(bar, cphase)) {
+                    if (clock64() - t0 > kWaitCycles) {
+                        s_err = 1;
+                        break;
+                    }
+                }
+            }
+        } else {
+            cp_async_wait<D - 1>();  // stage g has landed
+        }
         __syncwarp();
         const uint8_t* const sp = ring_p + (size_t)cslot * kSlot + (size_t)lane * kSB;
         const int sb = warp + k * nw;
@@ -241,29 +316,37 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
         __syncwarp();  // every lane is done with this slot before a later stage reuses it
 
         if (++k == spb) {
-            // tile done: per-lane partials of every warp meet in shared memory; one warp adds them in warp
-            // order and stores the tile's rows
-            float* const buf = red + (tcount & 1) * (kMaxWarps * 32);
-            buf[warp * 32 + lane] = PURE ? __uint_as_float(fold) : tot;
+            // tile done: this warp's per-lane partials go to the group buffer (double-buffered by group
+            // parity); after the group's last tile a CTA barrier, then for each tile of the group one warp,
+            // rotating with the tile, adds the partials in warp order and stores the tile's rows
+            const int gi = tcount % p.nb;
+            float* const gbuf = red + ((tcount / p.nb) & 1) * (kGroupMax * kMaxWarps * 32);
+            gbuf[(gi * kMaxWarps + warp) * 32 + lane] = PURE ? __uint_as_float(fold) : tot;
             tot = 0.f;
             fold = 0u;
-            __syncthreads();
-            if (warp == tcount % nw) {
-                const int r0 = tile * TR;
-                if constexpr (PURE) {
-                    uint32_t f = 0u;
-                    for (int w = 0; w < nw; ++w) f ^= __float_as_uint(buf[w * 32 + lane]);
-                    const int rr = lane % TR;
-                    if (r0 + rr < p.N) (NS == 2 && lane >= TR ? p.y1 : p.y0)[r0 + rr] = __uint_as_float(f);
-                } else {
-                    float v = 0.f;
-                    for (int w = 0; w < nw; ++w) v += buf[w * 32 + lane];
-                    const int rr = lane % TR;
-                    if (NS == 2 && p.swiglu) {
-                        const float up = __shfl_down_sync(0xffffffffu, v, TR);
-                        if (lane < TR && r0 + rr < p.N) p.y0[r0 + rr] = silu(v) * up;
-                    } else if (r0 + rr < p.N) {
-                        (NS == 2 && lane >= TR ? p.y1 : p.y0)[r0 + rr] = v;
+            if (gi == p.nb - 1 || tcount == my_tiles - 1) {
+                __syncthreads();
+                for (int i = 0; i <= gi; ++i) {
+                    if (warp != (tcount - gi + i) % nw) continue;
+                    const float* const buf = gbuf + i * (kMaxWarps * 32);
+                    const bool bad = *reinterpret_cast<volatile int*>(&s_err) != 0;
+                    const int r0 = (tile - (gi - i) * (int)gridDim.x) * TR;
+                    if constexpr (PURE) {
+                        uint32_t f = 0u;
+                        for (int w = 0; w < nw; ++w) f ^= __float_as_uint(buf[w * 32 + lane]);
+                        const int rr = lane % TR;
+                        if (r0 + rr < p.N) (NS == 2 && lane >= TR ? p.y1 : p.y0)[r0 + rr] = bad ? NAN : __uint_as_float(f);
+                    } else {
+                        float v = 0.f;
+                        for (int w = 0; w < nw; ++w) v += buf[w * 32 + lane];
+                        if (bad) v = NAN;
+                        const int rr = lane % TR;
+                        if (NS == 2 && p.swiglu) {
+                            const float up = __shfl_down_sync(0xffffffffu, v, TR);
+                            if (lane < TR && r0 + rr < p.N) p.y0[r0 + rr] = silu(v) * up;
+                        } else if (r0 + rr < p.N) {
+                            (NS == 2 && lane >= TR ? p.y1 : p.y0)[r0 + rr] = v;
+                        }
                     }
                 }
             }
@@ -271,16 +354,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const RowPa
             tile += (int)gridDim.x;
             ++tcount;
         }
-        cslot = cslot + 1 == D ? 0 : cslot + 1;
+        if (++cslot == D) {
+            cslot = 0;
+            cphase ^= 1u;
+        }
     }
 }
 
 inline uint32_t round_up_u32(uint32_t a, uint32_t b) { return (a + b - 1) / b * b; }
 
-template <int NS, int D, bool PURE>
+template <int NS, int D, bool PURE, bool TMA>
 cudaError_t launch_rows_fixed(const DeviceInfo& di, const RowParams& p, int nw, uint32_t smem, cudaStream_t s) {
     static std::once_flag attr_once[64];
-    auto kern = q4k_rows_kernel<NS, D, PURE>;
+    auto kern = q4k_rows_kernel<NS, D, PURE, TMA>;
     cudaError_t err = cudaSuccess;
     std::call_once(attr_once[di.device & 63], [&] {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
@@ -290,22 +376,86 @@ cudaError_t launch_rows_fixed(const DeviceInfo& di, const RowParams& p, int nw, 
     return launch_kernel(kern, grid, nw * 32, smem, s, p);
 }
 
-// Developer override of the ring depth and warp count, read once from Q4GEMV_Q4K_ROWS="depth,warps". Used
-// for tuning sweeps; the defaults come from such sweeps.
-void rows_override(int* depth, int* warps) {
-    static int o_d = -1, o_w = -1;
+// Developer override of the ring depth, warp count, reduction group and copy engine (1: bulk tensor copies,
+// 0: per-lane cp.async), read once from Q4GEMV_Q4K_ROWS="depth,warps,group,tma". Used for tuning sweeps;
+// the defaults come from such sweeps.
+void rows_override(int* depth, int* warps, int* group, int* tma) {
+    static int o_d = -1, o_w = -1, o_g = -1, o_t = -1;
     static std::once_flag once;
     std::call_once(once, [] {
         const char* e = getenv("Q4GEMV_Q4K_ROWS");
-        if (e) sscanf(e, "%d,%d", &o_d, &o_w);
+        if (e) sscanf(e, "%d,%d,%d,%d", &o_d, &o_w, &o_g, &o_t);
     });
     if (o_d > 0) *depth = o_d;
     if (o_w > 0) *warps = o_w;
+    if (o_g > 0) *group = o_g;
+    if (o_t >= 0) *tma = o_t;
 }
 
-// Shared memory: [staged xhat K*4][(S_j, 2^(22+e_j)) per sub-block][reduction 2*16*32 + 16 floats]
-//                [nw rings of D slots of 4608 bytes]. Warps: the super-blocks per row spread evenly over at
-// most 16 warps; depth: the deepest of 4, 3, 2 that fits.
+// Tensor map of a Q4_K weight matrix as a 2-D byte tensor [N][K/256*144], box 144 bytes x `rows`, rows past
+// N zero-filled. The encoder comes from the driver through the runtime's entry-point query; maps are cached
+// per (matrix, N, K, rows) since encoding one costs host time on every call otherwise.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+struct MapEntry {
+    const void* w = nullptr;
+    int N = 0, K = 0, rows = 0;
+    CUtensorMap map;
+};
+
+bool weight_map(CUtensorMap* out, const uint8_t* w, int N, int K, int rows) {
+    static std::mutex mu;
+    static MapEntry cache[16];
+    static int next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const MapEntry& m : cache)
+        if (m.w == w && m.N == N && m.K == K && m.rows == rows) {
+            *out = m.map;
+            return true;
+        }
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t row_bytes = (cuuint64_t)(K / 256) * kSB;
+    const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)kSB, (cuuint32_t)rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    MapEntry& e = cache[next];
+    if (fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        e.w = nullptr;
+        return false;
+    }
+    e.w = w;
+    e.N = N;
+    e.K = K;
+    e.rows = rows;
+    *out = e.map;
+    next = (next + 1) % 16;
+    return true;
+}
+
+// Shared memory: [staged xhat K*4][(S_j, 2^(22+e_j)) per sub-block][reduction 2*4*16*32 + 16 floats]
+//                [mbarriers 16*3*8, error word][nw rings of D slots of 4608 bytes]. Warps: the super-blocks per row
+// spread evenly over at most 16 warps; depth: 2 (3 on request) if it fits, fewer warps for the longest
+// inputs (up to K = 48384).
 template <int NS, bool PURE>
 cudaError_t run_rows(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x, const float* gamma,
                      float eps, int N, int K, bool swiglu, cudaStream_t s) {
@@ -325,21 +475,29 @@ cudaError_t run_rows(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1,
     p.K = K;
     p.nsb = K / 256;
     p.tiles = (N + 32 / NS - 1) / (32 / NS);
-    int depth = 3, want_w = kMaxWarps;
-    rows_override(&depth, &want_w);
+    int depth = 2, want_w = kMaxWarps, nb = kGroupMax, tma = 1;
+    rows_override(&depth, &want_w, &nb, &tma);
+    p.nb = std::max(1, std::min(kGroupMax, nb));
+    if (tma) {
+        if (!weight_map(&p.tm0, w0, N, K, 32 / NS)) return cudaErrorNotSupported;
+        if (NS == 2 && !weight_map(&p.tm1, w1, N, K, 32 / NS)) return cudaErrorNotSupported;
+    }
     const int per_warp = (p.nsb + std::min(want_w, kMaxWarps) - 1) / std::min(want_w, kMaxWarps);
     const int nw = (p.nsb + per_warp - 1) / per_warp;
     p.xs_off = 0;
     p.ss_off = PURE ? 0u : (uint32_t)K * 4u;
     p.red_off = p.ss_off + (PURE ? 0u : round_up_u32((uint32_t)(K / 32) * 8u, 128u));
-    p.slots_off = p.red_off + round_up_u32((uint32_t)(2 * kMaxWarps * 32 + kMaxWarps) * 4u, 128u);
-    for (int dd = std::min(4, std::max(2, depth)); dd >= 2; --dd) {
-        const uint32_t smem = p.slots_off + (uint32_t)(nw * dd) * kSlot;
-        if (smem > (uint32_t)di.max_smem_optin) continue;
-        switch (dd) {
-            case 4: return launch_rows_fixed<NS, 4, PURE>(di, p, nw, smem, s);
-            case 3: return launch_rows_fixed<NS, 3, PURE>(di, p, nw, smem, s);
-            default: return launch_rows_fixed<NS, 2, PURE>(di, p, nw, smem, s);
+    p.bar_off = p.red_off + round_up_u32((uint32_t)(2 * kGroupMax * kMaxWarps * 32 + kMaxWarps) * 4u, 128u);
+    p.slots_off = p.bar_off + round_up_u32((uint32_t)(kMaxWarps * 3 * 8 + 4), 128u);
+    for (int w = nw; w >= 1; --w) {
+        for (int dd = std::min(3, std::max(2, depth)); dd >= 2; --dd) {
+            const uint32_t smem = p.slots_off + (uint32_t)(w * dd) * kSlot;
+            if (smem > (uint32_t)di.max_smem_optin) continue;
+            if (dd == 3)
+                return tma ? launch_rows_fixed<NS, 3, PURE, true>(di, p, w, smem, s)
+                           : launch_rows_fixed<NS, 3, PURE, false>(di, p, w, smem, s);
+            return tma ? launch_rows_fixed<NS, 2, PURE, true>(di, p, w, smem, s)
+                       : launch_rows_fixed<NS, 2, PURE, false>(di, p, w, smem, s);
         }
     }
     return cudaErrorNotSupported;

@@ -56,7 +56,6 @@ struct RowParams {
     uint32_t xs_off, ss_off, red_off, bar_off, slots_off;
 };
 
-constexpr long long kWaitCycles = 4000000000LL;  // bound on one wait for a stage (about two seconds)
 
 // byte j of w as an exact float (0x4B000000 | b is 2^23 + b)
 __device__ __forceinline__ float sbyte(uint32_t w, int j) {
@@ -68,21 +67,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n selp.u32 %0, 1, 0, P;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0u;
-}
 // 2-D tensor tile (x bytes in, y rows down) into shared memory, completing on the mbarrier's transaction count
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
                                             uint64_t policy) {
@@ -248,16 +232,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
         issue();  // stage g + D - 1 into the slot consumed at g - 1
         if constexpr (TMA) {
             // stage g has landed once its slot's mbarrier completes phase cphase; the wait is bounded
-            const uint32_t bar = bars + 8u * (uint32_t)cslot;
-            if (!mbar_try_wait(bar, cphase)) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(bar, cphase)) {
-                    if (clock64() - t0 > kWaitCycles) {
-                        s_err = 1;
-                        break;
-                    }
-                }
-            }
+            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
         } else {
             cp_async_wait<D - 1>();  // stage g has landed
         }

@@ -41,7 +41,8 @@ struct Q4Params {
     int S;      // chunks per row
     int jobs;   // row groups of R rows
     int dcopy;  // scales travel in the slot (else each unit reads its scale from global memory)
-    uint32_t xs_off, aux_off, slots_off;
+    int bulk;   // every stage is whole rows: one bulk copy each for quants and scales, on a slot mbarrier
+    uint32_t xs_off, aux_off, bar_off, slots_off;
 };
 
 __host__ __device__ constexpr uint32_t round_up_u(uint32_t a, uint32_t b) { return (a + b - 1) / b * b; }
@@ -74,6 +75,18 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     const uint32_t xs = s_base + p.xs_off;
     const uint32_t aux = s_base + p.aux_off;
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
+    const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot (bulk mode)
+    // set when a stage wait ran out: the CTA's rows are then stored as NaN
+    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + W * D * 8);
+    if (threadIdx.x == 0) s_err = 0;
+    if (p.bulk) {
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < D; ++k) mbar_init(bars + 8u * k, 1u);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
 
     // Warps are numbered across CTAs first so that a small job count still spreads over all SMs.
     const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
@@ -90,7 +103,17 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
             const int b0 = ic * CB;
             const int nb = min(CB, p.nblk - b0);
             const uint32_t slot = ring + (uint32_t)islot * SLOT;
-            if (nb == CB && p.S == 1) {
+            if (p.bulk) {
+                // lane 0 moves the rows' quants and scales; this warp's earlier reads of the slot are ordered
+                // before the asynchronous write
+                if (lane == 0) {
+                    const uint32_t bar = bars + 8u * (uint32_t)islot;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(bar, (uint32_t)rv * (QROW + CB * 2));
+                    bulk_copy(slot, p.qs + (size_t)r0 * QROW, (uint32_t)rv * QROW, bar, pol);
+                    bulk_copy(slot + QBYTES, p.d + (size_t)r0 * CB, (uint32_t)(rv * CB * 2), bar, pol);
+                }
+            } else if (nb == CB && p.S == 1) {
                 warp_copy_async(slot, p.qs + (size_t)r0 * QROW, (uint32_t)rv * QROW, lane, pol);
                 if (p.dcopy)
                     warp_copy_async(slot + QBYTES, p.d + (size_t)r0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
@@ -109,7 +132,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
             }
             islot = islot + 1 == D ? 0 : islot + 1;
         }
-        cp_async_commit();
+        if (!p.bulk) cp_async_commit();
     };
 
 #pragma unroll
@@ -192,9 +215,15 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     const int my_jobs = gw < p.jobs ? (p.jobs - 1 - gw) / Wtot + 1 : 0;
     const int total = my_jobs * p.S;
     int job = gw, c = 0, cslot = 0;
+    uint32_t cphase = 0u;
     for (int g = 0; g < total; ++g) {
-        issue();                 // stage g + D - 1 into the slot consumed at g - 1
-        cp_async_wait<D - 1>();  // stage g has landed
+        issue();  // stage g + D - 1 into the slot consumed at g - 1
+        // stage g has landed: its slot's mbarrier completed phase cphase (bounded wait), or its commit group
+        if (p.bulk) {
+            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
+        } else {
+            cp_async_wait<D - 1>();
+        }
         __syncwarp();
         const uint8_t* const slot_p = ring_p + cslot * SLOT;
         const int r0 = job * R;
@@ -297,7 +326,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 for (int r = 0; r < R; ++r) {
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) fold[r] ^= __shfl_xor_sync(0xffffffffu, fold[r], off);
-                    if (lane == 0 && r < rv) p.y[r0 + r] = __uint_as_float(fold[r]);
+                    if (lane == 0 && r < rv)
+                        p.y[r0 + r] = *reinterpret_cast<volatile int*>(&s_err) ? NAN : __uint_as_float(fold[r]);
                     fold[r] = 0u;
                 }
             } else {
@@ -320,7 +350,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 if (leader && idx < NV) {
                     const int r = idx / V;
                     const int v = idx - r * V;
-                    if (r < rv) p.y[(size_t)v * p.N + r0 + r] = vals[0];
+                    if (r < rv)
+                        p.y[(size_t)v * p.N + r0 + r] = *reinterpret_cast<volatile int*>(&s_err) ? NAN : vals[0];
                 }
             }
         }
@@ -328,8 +359,22 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
             c = 0;
             job += Wtot;
         }
-        cslot = cslot + 1 == D ? 0 : cslot + 1;
+        if (++cslot == D) {
+            cslot = 0;
+            cphase ^= 1u;
+        }
     }
+}
+
+// Developer switch back to per-lane cp.async copies for whole-row stages, read once from Q4GEMV_Q4_BULK=0.
+inline bool bulk_off() {
+    static bool off = false;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* e = getenv("Q4GEMV_Q4_BULK");
+        off = e && e[0] == '0';
+    });
+    return off;
 }
 
 // Developer override of the ring depth, read once from Q4GEMV_Q4_DEPTH. Used for tuning sweeps; the
@@ -351,7 +396,8 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     const uint32_t nblk = (uint32_t)K / 32u;
     const uint32_t xsb = PURE ? 0u : xs_chunk_bytes((uint32_t)V, nblk);
     const uint32_t axb = PURE ? 0u : aux_bytes((uint32_t)V, nblk);
-    const uint32_t smem = xsb + axb + (uint32_t)(W * D) * slot_bytes<R, UPL>();
+    const uint32_t barb = round_up_u((uint32_t)(W * D * 8 + 4), 128u);  // slot mbarriers and the error word
+    const uint32_t smem = xsb + axb + barb + (uint32_t)(W * D) * slot_bytes<R, UPL>();
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     if (XREG && (int)nblk > CB) return cudaErrorNotSupported;
     auto kern = q4_gemv_kernel<V, R, W, D, UPL, XREG, PURE, NCH>;
@@ -372,9 +418,11 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     p.S = (int)((nblk + CB - 1) / CB);
     p.jobs = (N + R - 1) / R;
     p.dcopy = dcopy ? 1 : 0;
+    p.bulk = (dcopy && p.S == 1 && (int)nblk == CB && !bulk_off()) ? 1 : 0;
     p.xs_off = 0;
     p.aux_off = xsb;
-    p.slots_off = xsb + axb;
+    p.bar_off = xsb + axb;
+    p.slots_off = xsb + axb + barb;
     const int grid = std::min(di.sm_count, p.jobs);
     return launch_kernel(kern, grid, W * 32, smem, s, p);
 }

@@ -55,7 +55,8 @@ struct MoEParams {
     int ms;    // routing table stride: T*topk rounded up to 32
     int deal;  // 1: jobs dealt round-robin over the warps; 0: contiguous cost-balanced ranges
     int cost_a, cost_b;
-    uint32_t route_off, xs_off, aux_off, slots_off;
+    int bulk;  // every stage is whole rows: bulk copies of quants and scales on a slot mbarrier
+    uint32_t route_off, xs_off, aux_off, bar_off, slots_off;
     unsigned* fault;
 };
 
@@ -227,6 +228,18 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const uint32_t xs = s_base + p.xs_off;
     const uint32_t aux = s_base + p.aux_off;
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
+    const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot (bulk mode)
+    // set when a stage wait ran out: the CTA's outputs are then stored as NaN
+    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + W * D * 8);
+    if (threadIdx.x == 0) s_err = 0;
+    if (p.bulk) {
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < D; ++k) mbar_init(bars + 8u * k, 1u);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
     const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
     const int jobs = ngroups * NP * rgs;
@@ -322,6 +335,12 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             const int nb = min(CB, p.nblk - b0);
             const size_t row0 = (size_t)e * p.N + r0;
             const uint32_t slot = ring + (uint32_t)islot * SLOT;
+            if (p.bulk && lane == 0) {
+                // this warp's earlier reads of the slot are ordered before the asynchronous writes
+                const uint32_t bar = bars + 8u * (uint32_t)islot;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_expect_tx(bar, (uint32_t)((SWIGLU ? 2 : 1) * rv) * (QROW + CB * 2));
+            }
 #pragma unroll
             for (int sp = 0; sp < (SWIGLU ? 2 : 1); ++sp) {
                 const int proj = SWIGLU ? sp : ik.sp;
@@ -329,7 +348,13 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                 const uint16_t* d = proj == 0 ? p.dg : p.du;
                 const uint32_t qdst = slot + (uint32_t)(sp * R) * QROW;
                 const uint32_t ddst = slot + QBYTES + (uint32_t)(sp * R * CB * 2);
-                if (nb == CB && p.S == 1) {
+                if (p.bulk) {
+                    if (lane == 0) {
+                        const uint32_t bar = bars + 8u * (uint32_t)islot;
+                        bulk_copy(qdst, q + row0 * QROW, (uint32_t)rv * QROW, bar, pol);
+                        bulk_copy(ddst, d + row0 * CB, (uint32_t)(rv * CB * 2), bar, pol);
+                    }
+                } else if (nb == CB && p.S == 1) {
                     warp_copy_async(qdst, q + row0 * QROW, (uint32_t)rv * QROW, lane, pol);
                     if (p.dcopy) warp_copy_async(ddst, d + row0 * CB, (uint32_t)(rv * CB * 2), lane, pol);
                 } else {
@@ -345,7 +370,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             ++issued;
             islot = islot + 1 == D ? 0 : islot + 1;
         }
-        cp_async_commit();
+        if (!p.bulk) cp_async_commit();
     };
 
 #pragma unroll
@@ -403,10 +428,17 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 
     Cursor k = cursor_at(j0);
     int cslot = 0;
+    uint32_t cphase = 0u;
     for (int g = 0; g < total; ++g) {
-        issue();                 // stage g + D - 1 into the slot consumed at g - 1
-        cp_async_wait<D - 1>();  // stage g has landed
+        issue();  // stage g + D - 1 into the slot consumed at g - 1
+        // stage g has landed: its slot's mbarrier completed phase cphase (bounded wait), or its commit group
+        if (p.bulk) {
+            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
+        } else {
+            cp_async_wait<D - 1>();
+        }
         __syncwarp();
+        const bool bad = *reinterpret_cast<volatile int*>(&s_err) != 0;
         const uint32_t slot = ring + (uint32_t)cslot * SLOT;
         const int grp = gorder[k.grp];
         const int gc = group_cnt[grp];
@@ -497,7 +529,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     for (int r = 0; r < R; ++r) {
 #pragma unroll
                         for (int off = 16; off >= 1; off >>= 1) fold[r] ^= __shfl_xor_sync(0xffffffffu, fold[r], off);
-                        if (lane < cnt && r < rv) y[(size_t)list[first + lane] * p.N + r0 + r] = __uint_as_float(fold[r]);
+                        if (lane < cnt && r < rv)
+                            y[(size_t)list[first + lane] * p.N + r0 + r] = bad ? NAN : __uint_as_float(fold[r]);
                         fold[r] = 0u;
                     }
                 } else {
@@ -523,12 +556,12 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                         if (leader && idx < R * C) {
                             const int r = idx / C;
                             const int m = idx - r * C;
-                            if (r < rv) p.yg[(size_t)list[first + m] * p.N + r0 + r] = silu(vals[0]) * up;
+                            if (r < rv) p.yg[(size_t)list[first + m] * p.N + r0 + r] = bad ? NAN : silu(vals[0]) * up;
                         }
                     } else if (leader && idx < NV) {
                         const int r = idx / C;
                         const int m = idx - r * C;
-                        if (r < rv) y[(size_t)list[first + m] * p.N + r0 + r] = vals[0];
+                        if (r < rv) y[(size_t)list[first + m] * p.N + r0 + r] = bad ? NAN : vals[0];
                     }
                 }
             }
@@ -544,7 +577,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             }
         }
         advance(k);
-        cslot = cslot + 1 == D ? 0 : cslot + 1;
+        if (++cslot == D) {
+            cslot = 0;
+            cphase ^= 1u;
+        }
     }
 }
 
@@ -579,6 +615,17 @@ unsigned* fault_word(int device) {
     return ptrs[device & 63];
 }
 
+// Developer switch back to per-lane cp.async copies for whole-row stages, read once from Q4GEMV_MOE_BULK=0.
+bool bulk_off() {
+    static bool off = false;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* e = getenv("Q4GEMV_MOE_BULK");
+        off = e && e[0] == '0';
+    });
+    return off;
+}
+
 template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     const uint32_t route = (uint32_t)round_up(route_ints(p.ms) * 4, 128);
@@ -587,10 +634,12 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     p.route_off = 0;
     p.xs_off = route;
     p.aux_off = route + xsb;
-    p.slots_off = route + xsb + axb;
+    p.bar_off = route + xsb + axb;
+    p.slots_off = p.bar_off + (uint32_t)round_up(W * D * 8 + 4, 128);  // slot mbarriers and the error word
     const uint32_t smem = p.slots_off + (uint32_t)(W * D) * moe_slot_bytes(SWIGLU ? 2 * R : R, UPL);
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     p.S = (p.nblk + 32 * UPL - 1) / (32 * UPL);
+    p.bulk = (p.dcopy && p.S == 1 && p.nblk == 32 * UPL && !bulk_off()) ? 1 : 0;
     auto kern = moe_q4_kernel<R, W, D, UPL, PURE, SWIGLU>;
     static std::once_flag attr_once[64];
     cudaError_t err = cudaSuccess;

@@ -34,7 +34,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = ["device_common.cuh", "launch.h", "q4_dense.cuh", "kernels_q4.cu", "kernels_q4_v2_4.cu",
-                  "kernels_q4_v5_8.cu", "kernels_q4k.cu", "kernels_q4k_rows.cu", "kernels_moe.cu", "kernels_router.cu"]
+                  "kernels_q4_v5_8.cu", "kernels_q4_v9_16.cu", "kernels_q4k.cu", "kernels_q4k_rows.cu",
+                  "kernels_q4k_batched.cu", "kernels_moe.cu", "kernels_router.cu"]
 
 
 # ------------------------------------------------------------------------------------------------

@@ -17,7 +17,9 @@
  *      Q4_EUNSUPPORTED the current device is not sm_103, or the staged input (M*K*4 bytes, T*K*4 for MoE)
  *                      does not fit in one CTA's shared memory next to the weight rings
  *    q4_last_error() describes the most recent refusal or failure of the calling thread.
- *  - Kernels never trap and contain no spin loops: each warp waits only for its own asynchronous copies.
+ *  - Kernels never trap and contain no unbounded waits: each warp waits only for its own asynchronous copies
+ *    (cp.async groups, or an mbarrier that its bulk copies complete). An mbarrier wait gives up after about
+ *    4e9 SM cycles; the rows of every CTA in which that happened are then written as NaN.
  *  - Inputs are fp32 vectors, outputs fp32. Weights are packed as described per format below; multi-byte
  *    fields are little-endian.
  *

@@ -586,9 +586,11 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b"
-// (variant 48: 4 rows x 8 warps; 216: 2 rows x 16 warps; job cost cost_a + cost_b * C). Used for tuning
-// sweeps; the defaults come from such sweeps.
+// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b,deal"
+// (variant 48: 4 rows x 8 warps; 416: 4 rows x 16 warps; 412: 4 rows x 12 warps; 216: 2 rows x 16 warps; the
+// SwiGLU form: 84: 4+4 rows x 8 warps, 416: 2+2 rows x 16 warps, 412: 2+2 rows x 12 warps, 216: 1+1 rows x 16
+// warps, otherwise 2+2 rows x 8 warps; job cost cost_a + cost_b * C; deal 1: round-robin, 0: contiguous
+// ranges). Used for tuning sweeps; the defaults come from such sweeps.
 void plan_override(int* variant, int* depth, int* cost_a, int* cost_b, int* deal) {
     static int o_v = -1, o_d = -1, o_a = -1, o_b = -1, o_deal = -1;
     static std::once_flag once;
@@ -701,18 +703,32 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
               ((reinterpret_cast<uintptr_t>(d_up) & 15u) == 0);
     p.fault = fault_word(di.device);
     if (!p.fault) return cudaErrorInvalidSymbol;
-    int variant = 48, depth = 3;
+    // defaults from sweeps over routing seeds: 16 warps x 4 rows, ring depth 2, contiguous cost-balanced job
+    // ranges; the SwiGLU form (4 gate + 4 up rows per slot) 8 warps with round-robin dealing
+    int variant = swiglu ? 84 : 416, depth = 2;
     p.cost_a = 9;
     p.cost_b = 5;
-    p.deal = 1;
+    p.deal = swiglu ? 1 : 0;
     plan_override(&variant, &depth, &p.cost_a, &p.cost_b, &p.deal);
-    if (pure_read) return variant == 216 ? launch<2, 16, true>(di, p, depth, s) : launch<4, 8, true>(di, p, depth, s);
+    if (pure_read) {
+        // the same streaming as the GEMV plan
+        if (variant == 216) return launch<2, 16, true>(di, p, depth, s);
+        if (variant == 416) return launch<4, 16, true>(di, p, depth, s);
+        return launch<4, 8, true>(di, p, depth, s);
+    }
     if (swiglu) {  // R gate + R up rows per slot
         if (variant == 216) return launch<1, 16, false, true>(di, p, depth, s);
         if (variant == 84) return launch<4, 8, false, true>(di, p, depth, s);
+        if (variant == 416) return launch<2, 16, false, true>(di, p, depth, s);
+        if (variant == 412) return launch<2, 12, false, true>(di, p, depth, s);
         return launch<2, 8, false, true>(di, p, depth, s);
     }
-    return variant == 216 ? launch<2, 16, false>(di, p, depth, s) : launch<4, 8, false>(di, p, depth, s);
+    switch (variant) {
+        case 216: return launch<2, 16, false>(di, p, depth, s);
+        case 416: return launch<4, 16, false>(di, p, depth, s);
+        case 412: return launch<4, 12, false>(di, p, depth, s);
+        default: return launch<4, 8, false>(di, p, depth, s);
+    }
 }
 
 cudaError_t read_and_clear_fault_moe(unsigned* out) {

@@ -11,12 +11,13 @@
 //    order of first appearance, and cut each expert's slot list into groups of at most kMaxC slots; slots
 //    with an id outside [0, E) get NaN outputs (written by CTA 0) and raise a status bit;
 //  * jobs are (group, projection, row group of R rows), numbered group-major; each warp owns one contiguous
-//    range of jobs, so it streams whole-row stages of consecutive rows through its own ring of cp.async
-//    slots with incremental control, and each selected expert's bytes are read once per call (once per
-//    group when more than kMaxC slots route to one expert);
+//    range of jobs (or jobs dealt round-robin), so it streams whole-row stages of consecutive rows through
+//    its own ring of slots (bulk copies on a slot mbarrier, or cp.async for chunked rows) with incremental
+//    control, and each selected expert's bytes are read once per call (once per group when more than kMaxC
+//    slots route to one expert);
 //  * all T input vectors are staged once per CTA, block by block, with the bias-free decode's per-block
-//    scaling (device_common.cuh): float[T][8 quads][K/32 units][4] and (2^(22+e), -8 * sum) pairs
-//    float2[T][K/32];
+//    scaling (device_common.cuh): float4[K/32 blocks / 32][T][8 quads][32] and (2^(22+e), -8 * sum) pairs
+//    float2[K/32 / 32][T][32], so a lane's quads of a token sit at constant offsets from one base per stage;
 //  * a job's slot count C (1..kMaxC) selects a compiled variant of the stage body, so each decoded code
 //    pair feeds exactly C packed FMAs; per block t = A * 2^(22+e) - 8 * sum(x), and the row accumulates
 //    d * t per routed slot;
@@ -84,7 +85,9 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 
 // SWIGLU: a job streams R gate rows and the same R up rows of its expert (one slot of 2R rows) and writes
 // silu(gate) * up per routed row; otherwise a job is R rows of one projection.
-template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
+// XG: the tokens are staged in groups of 32 blocks (K/32 a multiple of 32), so a lane's quads sit at constant
+// offsets; otherwise token-major with the quads K/32 * 16 bytes apart.
+template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU, bool XG>
 __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     static_assert(!(PURE && SWIGLU), "the pure-read instrument streams one projection per job");
     constexpr int NP = SWIGLU ? 1 : 2;      // jobs per (group, row group)
@@ -398,16 +401,21 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     float bsum, bmax;
                     block_sum_max(xv[j], bsum, bmax);
                     const int e = block_exponent(bmax);
+                    // XG layout: [group of 32 blocks][token][quad][block in group]; otherwise [token][quad][block]
+                    // (16 bytes each): the lanes of a warp read consecutive 16-byte pieces either way
+                    const int grp32 = u >> 5, ul = u & 31;
 #pragma unroll
                     for (int q8 = 0; q8 < 8; ++q8) {
                         const int hi = q8 >> 2;
-                        const uint32_t a = xs + (uint32_t)(((v * 8 + q8) * U + u) * 16);
+                        const uint32_t a = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q8) * 32 + ul) * 16
+                                                              : ((v * 8 + q8) * U + u) * 16);
                         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
                                      "f"(stage_scaled(xv[j][q8].x, hi, 0, e)), "f"(stage_scaled(xv[j][q8].y, hi, 1, e)),
                                      "f"(stage_scaled(xv[j][q8].z, hi, 2, e)), "f"(stage_scaled(xv[j][q8].w, hi, 3, e))
                                      : "memory");
                     }
-                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((v * U + u) * 8)),
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
+                                                                                            : v * U + u) * 8)),
                                  "f"(block_factor(e)), "f"(-8.0f * bsum)
                                  : "memory");
                 }
@@ -416,7 +424,6 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     }
     __syncthreads();
 
-    const uint32_t qstride = (uint32_t)U * 16u;  // bytes between the quads of one unit
     float tot[RR][kMaxC];
     uint32_t fold[RR];
 #pragma unroll
@@ -455,9 +462,20 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         // Stage body for C routed slots (compile-time), C = cnt.
         auto stage = [&](auto cc) {
             constexpr int C = decltype(cc)::value;
-            int tok[C];
+            // this lane's staged quads and block pairs of each routed token: from the stage's first group of 32
+            // blocks of that token (x_it, a_it: the step to the next group)
+            const float4* xq[C];
+            const float2* aq[C];
+            const int qs = XG ? 32 : U;  // quad stride (float4)
+            const int x_it = XG ? p.T * 8 * 32 : 32, a_it = XG ? p.T * 32 : 32;
 #pragma unroll
-            for (int m = 0; m < C; ++m) tok[m] = list[first + m] / p.topk;
+            for (int m = 0; m < C; ++m) {
+                const int tok = list[first + m] / p.topk;
+                xq[m] = reinterpret_cast<const float4*>(smem + p.xs_off) +
+                        (XG ? ((b0 >> 5) * p.T + tok) * 8 * 32 + lane : tok * 8 * U + b0 + lane);
+                aq[m] = reinterpret_cast<const float2*>(smem + p.aux_off) +
+                        (XG ? ((b0 >> 5) * p.T + tok) * 32 + lane : tok * U + b0 + lane);
+            }
 #pragma unroll 1
             for (int it = 0; it < UPL; ++it) {
                 const int ul = it * 32 + lane;
@@ -483,9 +501,6 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 #pragma unroll
                     for (int r = 0; r < RR; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
                 } else {
-                    uint32_t xa[C];
-#pragma unroll
-                    for (int m = 0; m < C; ++m) xa[m] = xs + ((uint32_t)tok[m] * 8u * (uint32_t)U + u) * 16u;
                     float2 acc[RR][C];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -495,8 +510,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                             d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
 #pragma unroll
                         for (int m = 0; m < C; ++m) {
-                            const float4 xl = lds128f(xa[m] + (uint32_t)i * qstride);
-                            const float4 xh = lds128f(xa[m] + (uint32_t)(4 + i) * qstride);
+                            const float4 xl = xq[m][it * x_it + i * qs];
+                            const float4 xh = xq[m][it * x_it + (4 + i) * qs];
 #pragma unroll
                             for (int r = 0; r < RR; ++r) {
                                 float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][m];
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     }
 #pragma unroll
                     for (int m = 0; m < C; ++m) {
-                        const float2 fa = lds64f(aux + ((uint32_t)tok[m] * (uint32_t)U + u) * 8u);
+                        const float2 fa = aq[m][it * a_it];
 #pragma unroll
                         for (int r = 0; r < RR; ++r) {
                             const float t = fmaf(acc[r][m].x + acc[r][m].y, fa.x, fa.y);
@@ -587,10 +602,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
 // Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b,deal"
-// (variant 48: 4 rows x 8 warps; 416: 4 rows x 16 warps; 412: 4 rows x 12 warps; 216: 2 rows x 16 warps; the
-// SwiGLU form: 84: 4+4 rows x 8 warps, 416: 2+2 rows x 16 warps, 412: 2+2 rows x 12 warps, 216: 1+1 rows x 16
-// warps, otherwise 2+2 rows x 8 warps; job cost cost_a + cost_b * C; deal 1: round-robin, 0: contiguous
-// ranges). Used for tuning sweeps; the defaults come from such sweeps.
+// (variant 416: 4 rows x 16 warps, otherwise 4 rows x 8 warps; the SwiGLU form: 84: 4+4 rows x 8 warps,
+// 216: 1+1 rows x 16 warps, otherwise 2+2 rows x 8 warps; depth: ignored, 2; job cost cost_a + cost_b * C; deal 1:
+// round-robin, 0: contiguous ranges). Used for tuning sweeps; the defaults come from such sweeps (12 warps,
+// 2 rows x 16 warps and depth 4 measured slower and are not compiled).
 void plan_override(int* variant, int* depth, int* cost_a, int* cost_b, int* deal) {
     static int o_v = -1, o_d = -1, o_a = -1, o_b = -1, o_deal = -1;
     static std::once_flag once;
@@ -628,6 +643,18 @@ bool bulk_off() {
     return off;
 }
 
+template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU, bool XG>
+cudaError_t launch_kernel_cfg(const DeviceInfo& di, const MoEParams& p, uint32_t smem, cudaStream_t s) {
+    auto kern = moe_q4_kernel<R, W, D, UPL, PURE, SWIGLU, XG>;
+    static std::once_flag attr_once[64];
+    cudaError_t err = cudaSuccess;
+    std::call_once(attr_once[di.device & 63], [&] {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+    });
+    if (err != cudaSuccess) return err;
+    return launch_kernel(kern, di.sm_count, W * 32, smem, s, p);
+}
+
 template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     const uint32_t route = (uint32_t)round_up(route_ints(p.ms) * 4, 128);
@@ -642,27 +669,22 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     p.S = (p.nblk + 32 * UPL - 1) / (32 * UPL);
     p.bulk = (p.dcopy && p.S == 1 && p.nblk == 32 * UPL && !bulk_off()) ? 1 : 0;
-    auto kern = moe_q4_kernel<R, W, D, UPL, PURE, SWIGLU>;
-    static std::once_flag attr_once[64];
-    cudaError_t err = cudaSuccess;
-    std::call_once(attr_once[di.device & 63], [&] {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-    });
-    if (err != cudaSuccess) return err;
-    return launch_kernel(kern, di.sm_count, W * 32, smem, s, p);
+    // grouped staging whenever the blocks fill whole groups of 32 (no padding); the pure read stages nothing
+    if constexpr (!PURE) {
+        if (p.nblk % 32 == 0) return launch_kernel_cfg<R, W, D, UPL, PURE, SWIGLU, true>(di, p, smem, s);
+    }
+    return launch_kernel_cfg<R, W, D, UPL, PURE, SWIGLU, false>(di, p, smem, s);
 }
 
+// Ring depth 2 (depths 3 and 4 measured no faster with the bulk copies and are not compiled).
 template <int R, int W, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_upl(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
-    cudaError_t e = cudaErrorNotSupported;
-    if (depth >= 4) e = launch_fixed<R, W, 4, UPL, PURE, SWIGLU>(di, p, s);
-    if (e == cudaErrorNotSupported && depth >= 3) e = launch_fixed<R, W, 3, UPL, PURE, SWIGLU>(di, p, s);
-    if (e == cudaErrorNotSupported) e = launch_fixed<R, W, 2, UPL, PURE, SWIGLU>(di, p, s);
-    return e;
+    (void)depth;
+    return launch_fixed<R, W, 2, UPL, PURE, SWIGLU>(di, p, s);
 }
 
 // Whole rows in one chunk up to K = 4096 (UPL = 1, 2, 4), longer rows in 128-block chunks; the deepest ring
-// that fits beside the routing tables and the staged tokens.
+// of depth 2 beside the routing tables and the staged tokens.
 template <int R, int W, bool PURE, bool SWIGLU = false>
 cudaError_t launch(const DeviceInfo& di, const MoEParams& p, int depth, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
@@ -710,25 +732,23 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.cost_b = 5;
     p.deal = swiglu ? 1 : 0;
     plan_override(&variant, &depth, &p.cost_a, &p.cost_b, &p.deal);
+    // 16 warps x 4 rows when it fits beside the staged tokens, else 8 warps x 4 rows (the same for the pure
+    // read, which streams like the GEMV plan)
+    e = cudaErrorNotSupported;
     if (pure_read) {
-        // the same streaming as the GEMV plan
-        if (variant == 216) return launch<2, 16, true>(di, p, depth, s);
-        if (variant == 416) return launch<4, 16, true>(di, p, depth, s);
-        return launch<4, 8, true>(di, p, depth, s);
+        if (variant == 416) e = launch<4, 16, true>(di, p, depth, s);
+        if (e == cudaErrorNotSupported) e = launch<4, 8, true>(di, p, depth, s);
+        return e;
     }
     if (swiglu) {  // R gate + R up rows per slot
         if (variant == 216) return launch<1, 16, false, true>(di, p, depth, s);
-        if (variant == 84) return launch<4, 8, false, true>(di, p, depth, s);
-        if (variant == 416) return launch<2, 16, false, true>(di, p, depth, s);
-        if (variant == 412) return launch<2, 12, false, true>(di, p, depth, s);
-        return launch<2, 8, false, true>(di, p, depth, s);
+        if (variant == 84) e = launch<4, 8, false, true>(di, p, depth, s);
+        if (e == cudaErrorNotSupported) e = launch<2, 8, false, true>(di, p, depth, s);
+        return e;
     }
-    switch (variant) {
-        case 216: return launch<2, 16, false>(di, p, depth, s);
-        case 416: return launch<4, 16, false>(di, p, depth, s);
-        case 412: return launch<4, 12, false>(di, p, depth, s);
-        default: return launch<4, 8, false>(di, p, depth, s);
-    }
+    if (variant == 416) e = launch<4, 16, false>(di, p, depth, s);
+    if (e == cudaErrorNotSupported) e = launch<4, 8, false>(di, p, depth, s);
+    return e;
 }
 
 cudaError_t read_and_clear_fault_moe(unsigned* out) {

@@ -38,7 +38,6 @@ static __device__ unsigned g_fault_moe;
 
 namespace {
 
-constexpr int kMaxSlots = 512;  // largest T * topk
 constexpr int kMaxC = 4;        // routed slots served per weight sweep
 
 struct MoEParams {
@@ -368,6 +367,13 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                             warp_copy_async(ddst + (uint32_t)(r * CB * 2), d + rb, (uint32_t)(nb * 2), lane, pol);
                     }
                 }
+                if (!p.dcopy) {
+                    // scales that cannot move by 16-byte copies (not 16-byte aligned, or K/32 not a multiple of
+                    // 8) go into the slot by plain loads, so the stage body always reads them from shared memory
+                    uint16_t* const ds = reinterpret_cast<uint16_t*>(smem + (ddst - s_base));
+                    for (int r = 0; r < rv; ++r)
+                        for (int u = lane; u < nb; u += 32) ds[r * CB + u] = __ldg(d + (row0 + r) * p.nblk + b0 + u);
+                }
             }
             advance(ik);
             ++issued;
@@ -450,7 +456,6 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         const int grp = gorder[k.grp];
         const int gc = group_cnt[grp];
         const int cnt = gc & 0xFF;
-        const int e = gc >> 8;
         const int first = group_first[grp];
         const int r0 = k.rg * R;
         const int rv = min(R, p.N - r0);
@@ -468,6 +473,9 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             const float2* aq[C];
             const int qs = XG ? 32 : U;  // quad stride (float4)
             const int x_it = XG ? p.T * 8 * 32 : 32, a_it = XG ? p.T * 32 : 32;
+            (void)qs;  // the pure read uses none of these
+            (void)x_it;
+            (void)a_it;
 #pragma unroll
             for (int m = 0; m < C; ++m) {
                 const int tok = list[first + m] / p.topk;
@@ -480,21 +488,14 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             for (int it = 0; it < UPL; ++it) {
                 const int ul = it * 32 + lane;
                 if (ul >= nb) continue;
-                const uint32_t u = (uint32_t)(b0 + ul);
                 uint4 w[RR];
                 float dsc[RR];
                 uint32_t dbits[RR];
 #pragma unroll
                 for (int r = 0; r < RR; ++r) {
                     // slot row r: projection (SWIGLU ? r / R : k.sp), expert row r0 + r % R
-                    const int rr = SWIGLU ? r % R : r;
                     w[r] = lds128(qb + (uint32_t)r * QROW + (uint32_t)(it * 512));
-                    if (p.dcopy) {
-                        dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
-                    } else {
-                        const uint16_t* dglob = (SWIGLU ? r >= R : k.sp != 0) ? p.du : p.dg;
-                        dbits[r] = rr < rv ? (uint32_t)__ldg(dglob + ((size_t)e * p.N + r0 + rr) * p.nblk + u) : 0u;
-                    }
+                    dbits[r] = lds_u16(db + (uint32_t)(r * CB * 2 + it * 64));
                     dsc[r] = f16_bits_to_f32(dbits[r]);
                 }
                 if constexpr (PURE) {

@@ -40,7 +40,7 @@ struct Q4Params {
     int N, K, nblk;
     int S;      // chunks per row
     int jobs;   // row groups of R rows
-    int dcopy;  // scales travel in the slot (else each unit reads its scale from global memory)
+    int dcopy;  // scales move by 16-byte copies (else the warp loads them into the slot itself)
     int bulk;   // every stage is whole rows: one bulk copy each for quants and scales, on a slot mbarrier
     uint32_t xs_off, aux_off, bar_off, slots_off;
 };
@@ -125,6 +125,14 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                         warp_copy_async(slot + QBYTES + (uint32_t)(r * CB * 2), p.d + rb, (uint32_t)(nb * 2), lane,
                                         pol);
                 }
+            }
+            if (!p.dcopy) {
+                // scales that cannot move by 16-byte copies (not 16-byte aligned, or K/32 not a multiple of 8)
+                // go into the slot by plain loads, so the unit loop always reads them from shared memory
+                uint16_t* const ds =
+                    reinterpret_cast<uint16_t*>(smem + p.slots_off + (size_t)(warp * D + islot) * SLOT + QBYTES);
+                for (int r = 0; r < rv; ++r)
+                    for (int u = lane; u < nb; u += 32) ds[r * CB + u] = __ldg(p.d + (size_t)(r0 + r) * p.nblk + b0 + u);
             }
             if (++ic == p.S) {
                 ic = 0;
@@ -242,10 +250,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 w[r] = qb[r * (QROW / 16) + it * 32];
-                if (p.dcopy)
-                    dbits[r] = db[r * CB + it * 32];
-                else
-                    dbits[r] = r < rv ? (uint32_t)__ldg(p.d + (size_t)(r0 + r) * p.nblk + b0 + it * 32 + lane) : 0u;
+                dbits[r] = db[r * CB + it * 32];
                 dsc[r] = f16_bits_to_f32(dbits[r]);
             }
             if constexpr (PURE) {

@@ -92,3 +92,23 @@ def test_moe_pure_read_touches_the_selected_experts():
 
 def test_no_fault_bits_after_the_suite():
     assert q4.q4_device_faults() == 0
+
+
+def test_moe_unaligned_scales_give_identical_rows():
+    """Scales only 2-byte aligned take the plain-load path into the slot; outputs equal the aligned call's."""
+    m = synth.make_moe(seed=21, E=16, N=200, K=2048, T=4, topk=4)
+    E, (T, topk), N = 16, m["ids"].shape, 200
+
+    def shifted(a):
+        flat = torch.from_numpy(np.ascontiguousarray(a).view(np.int16).ravel()).to("cuda")
+        buf = torch.zeros(flat.numel() + 8, dtype=torch.int16, device="cuda")
+        buf[1:1 + flat.numel()] = flat
+        return buf[1:1 + flat.numel()].view(torch.float16).view(a.shape)
+
+    outs = []
+    for dg, du in ((cu(m["d_gate"]), cu(m["d_up"])), (shifted(m["d_gate"]), shifted(m["d_up"]))):
+        yg, yu = Guarded(T, topk, N), Guarded(T, topk, N)
+        q4.moe_q4_gemv(yg.t, yu.t, cu(m["qs_gate"]), dg, cu(m["qs_up"]), du, cu(m["x"]), cu(m["ids"]), E)
+        outs.append((yg.result(), yu.result()))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -148,3 +148,26 @@ def test_refusals_on_device():
 
 def test_no_fault_bits_after_the_suite():
     assert q4.q4_device_faults() == 0
+
+
+def _offset_copy(a):
+    """The same values in device memory at a 2-byte offset from a 16-byte boundary (a view into a larger
+    buffer), so the scales cannot move by 16-byte copies."""
+    flat = torch.from_numpy(np.ascontiguousarray(a).view(np.int16).ravel()).to("cuda")
+    buf = torch.zeros(flat.numel() + 8, dtype=torch.int16, device="cuda")
+    buf[1:1 + flat.numel()] = flat
+    return buf[1:1 + flat.numel()].view(torch.float16).view(a.shape)
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_unaligned_scales_give_identical_rows(M):
+    """Scales that are only 2-byte aligned take the plain-load path into the slot; every row must equal, bit for
+    bit, the call with 16-byte aligned scales (same values, same summation order)."""
+    inp = synth.make_q4_gemv(seed=31 + M, N=1000, K=4096, M=M)
+    qs, X = cu(inp["qs"]), cu(inp["x"][:M])
+    d_al, d_un = cu(inp["d"]), _offset_copy(inp["d"])
+    assert d_un.data_ptr() % 16 == 2
+    Ya, Yu = Guarded(M, 1000), Guarded(M, 1000)
+    q4.q4_gemv_batched(Ya.t, qs, d_al, X)
+    q4.q4_gemv_batched(Yu.t, qs, d_un, X)
+    assert np.array_equal(Ya.result().view(np.uint32), Yu.result().view(np.uint32))

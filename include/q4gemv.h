@@ -112,7 +112,8 @@ int fused_rmsnorm_q4k_gemv(float *y, const uint8_t *w, const float *x, const flo
  * unfused Q4KGemvKernel); the batched contract of spark_model gemm_quant.rs, dense_gemv_batchm.
  *   Y float[M][N] (row-major), X float[M][K] (row-major, 16-byte aligned), w as fused_rmsnorm_q4k_gemv.
  *   1 <= M <= 8; N >= 1; K % 256 == 0. The M staged rows must fit in one CTA's shared memory beside the weight
- *   rings (M*K*4 + M*K/4 bytes: M = 8 up to K = 4096); larger inputs return Q4_EUNSUPPORTED.
+ *   rings (M*K*4 + M*K/4 bytes: M = 8 up to K = 4096); larger inputs return Q4_EUNSUPPORTED. M = 1 runs the
+ *   kernel of fused_rmsnorm_q4k_gemv without the normalisation, so its summation order differs from M >= 2.
  */
 int q4k_gemv_batched(float *Y, const uint8_t *w, const float *X, int M, int N, int K, q4_stream_t stream);
 

@@ -307,7 +307,10 @@ cudaError_t launch_q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, 
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
     switch (V) {
-        case 1: return run_batched<1, 2, 16>(di, Y, w, X, N, K, s);
+        case 1:
+            // one input: the row-per-lane kernel of the fused calls, without normalisation
+            e = launch_q4k_rows_gemv(Y, nullptr, w, nullptr, X, nullptr, 0.f, N, K, false, s);
+            return e == cudaErrorNotSupported ? run_batched<1, 2, 16>(di, Y, w, X, N, K, s) : e;
         case 2: return run_batched<2, 2, 16>(di, Y, w, X, N, K, s);
         case 3: return run_batched<3, 2, 8>(di, Y, w, X, N, K, s);
         case 4: return run_batched<4, 2, 8>(di, Y, w, X, N, K, s);

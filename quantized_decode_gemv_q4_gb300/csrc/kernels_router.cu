@@ -4,13 +4,17 @@
 // indices of the K largest logits and their softmax weights (optionally renormalised over the K). Here Wgate is
 // planar Q4 (E rows of K weights, the library's format) and x is fp32; one token per CTA row of the grid.
 //
-// Kernel shape (one CTA of 32 warps per token; the router matrix is small and stays in L2 after the first CTA):
-//  * stage the token's x block by block with the bias-free decode's per-block scaling (device_common.cuh);
-//  * warp w computes the logits of experts w, w + W, ... two rows at a time: lane l takes units l, l + 32, ...
-//    with 16-byte loads (four issued before use), one shift + eight ANDs per word and packed fp32x2 FMAs, folds
-//    each block with its scale, and the warp sums the lanes; logits go to shared memory;
-//  * warp 0 takes the softmax over all E logits (max subtracted) and K arg-max passes (ties to the lower
-//    index), writes ids and weights (and, when asked, the logits).
+// Kernel shape (one cluster of CS CTAs per token; the router matrix is small and stays in L2 after the first
+// cluster reads it):
+//  * every CTA stages the token's x block by block with the bias-free decode's per-block scaling
+//    (device_common.cuh);
+//  * CTA c of the cluster computes the logits of experts c, c + CS, ...: warp w takes experts c + CS*w,
+//    c + CS*(w + W), ... two rows at a time; lane l takes units l, l + 32, ... with 16-byte loads (four issued
+//    before use), one shift + eight ANDs per word and packed fp32x2 FMAs, folds each block with its scale, and
+//    the warp sums the lanes; the logits go to the CTA's own shared memory;
+//  * after a cluster barrier, CTA 0 gathers the other CTAs' logits through distributed shared memory; a second
+//    barrier releases them; its warp 0 then takes the softmax over all E logits (max subtracted) and K arg-max
+//    passes (ties to the lower index), and writes ids and weights (the logits, when asked, come from every CTA).
 #include <algorithm>
 #include <mutex>
 
@@ -32,12 +36,31 @@ struct RouterParams {
     uint32_t xs_off, aux_off, lg_off;
 };
 
-template <int W>
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster: writes before the barrier are visible to reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float in CTA `rank`'s shared memory at this CTA's shared address `local`.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int W, int CS>
 __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int t = blockIdx.x;
+    const int t = (int)blockIdx.x / CS;
+    const int c = (int)cluster_ctarank();
     const uint32_t s_base = smem_addr(smem);
     const uint32_t xs = s_base + p.xs_off;
     const uint32_t aux = s_base + p.aux_off;
@@ -76,10 +99,11 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
     }
     __syncthreads();
 
-    // logits: warp w takes experts w and w + W, then w + 2W and w + 3W, ...; lane l units l and l + 32, then
-    // l + 64 and l + 96, ...; the four (row, unit) loads of a step are issued before any is used
-    for (int e0 = warp; e0 < p.E; e0 += 2 * W) {
-        const int ea = e0, eb = e0 + W;
+    // logits of this CTA's experts: warp w takes c + CS*w and c + CS*(w + W), then the next two ...; lane l
+    // units l and l + 32, then l + 64 and l + 96, ...; the four (row, unit) loads of a step are issued before
+    // any is used
+    for (int e0 = c + CS * warp; e0 < p.E; e0 += 2 * CS * W) {
+        const int ea = e0, eb = e0 + CS * W;
         const bool hb = eb < p.E;
         float ta = 0.f, tb = 0.f;
         for (int u0 = lane; u0 < p.nblk; u0 += 64) {
@@ -132,9 +156,18 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
             }
         }
     }
+    // every CTA's logits are in its shared memory; CTA 0 gathers them, then the cluster may exit
+    cluster_sync();
+    if (c == 0) {
+        const uint32_t lg_addr = smem_addr(lg);
+        for (int e = threadIdx.x; e < p.E; e += W * 32)
+            if (e % CS != 0) lg[e] = ld_cluster_f32(lg_addr + 4u * (uint32_t)e, (uint32_t)(e % CS));
+    }
+    cluster_sync();
+    if (c != 0) return;
     __syncthreads();
 
-    // softmax over all E logits and the top K (warp 0)
+    // softmax over all E logits and the top K (warp 0 of CTA 0)
     if (warp == 0) {
         float mx = -INFINITY;
         for (int e = lane; e < p.E; e += 32) mx = fmaxf(mx, lg[e]);
@@ -198,7 +231,7 @@ cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
-    constexpr int W = 32;
+    constexpr int W = 8, CS = 8;
     RouterParams p;
     p.ids = ids;
     p.weights = weights;
@@ -219,13 +252,28 @@ cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const
     p.lg_off = xsb + axb;
     const uint32_t smem = p.lg_off + (uint32_t)E * 4u;
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
-    auto kern = moe_router_kernel<W>;
+    auto kern = moe_router_kernel<W, CS>;
     static std::once_flag attr_once[64];
     std::call_once(attr_once[di.device & 63], [&] {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
     });
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, T, W * 32, smem, s, p);
+    // one cluster of CS CTAs per token (CS = 8 is the portable cluster size)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(T * CS));
+    cfg.blockDim = dim3((unsigned)(W * 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_overlap() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace q4

@@ -62,10 +62,9 @@ struct MoEParams {
 
 // Routing tables in shared memory (route_off), each of ms = T*topk rounded up to 32 entries: slot_ids, rank,
 // owner, ucount, uoffset (ms+1), list, group_ux, group_first, group_cnt, scalars[4] (number of distinct experts,
-// number of groups), then the cumulative job cost gcum[ms+1] (64-bit) and the job order of the groups gorder
-// (groups sorted by slot
-// count).
-__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + ms; }
+// number of groups), then the cumulative job cost gcum[ms+1] (64-bit), the job order of the groups gorder
+// (groups sorted by slot count) and the token of each list entry ltok.
+__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 2 * ms; }
 
 // Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
 // (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
@@ -115,6 +114,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     int* scalars = route + 9 * ms + 1;
     long long* gcum = reinterpret_cast<long long*>(route + 9 * ms + 8);  // 8-byte aligned (ms % 32 == 0)
     int* gorder = route + 9 * ms + 8 + 2 * (ms + 1) + 2;
+    int* ltok = gorder + ms;  // token of each list entry (slot / topk), so stages divide nothing
 
     // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
     // in the stream (it may have written ids, x or the outputs) before anything else.
@@ -201,7 +201,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const int ngroups = scalars[1];
     for (int i = threadIdx.x; i < TK; i += kThreads) {
         const int ux = owner[i];
-        if (ux >= 0) list[uoffset[ux] + rank[i]] = i;
+        if (ux >= 0) {
+            list[uoffset[ux] + rank[i]] = i;
+            ltok[uoffset[ux] + rank[i]] = i / p.topk;
+        }
     }
     __syncthreads();
     // group -> expert id
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             (void)a_it;
 #pragma unroll
             for (int m = 0; m < C; ++m) {
-                const int tok = list[first + m] / p.topk;
+                const int tok = ltok[first + m];
                 xq[m] = reinterpret_cast<const float4*>(smem + p.xs_off) +
                         (XG ? ((b0 >> 5) * p.T + tok) * 8 * 32 + lane : tok * 8 * U + b0 + lane);
                 aq[m] = reinterpret_cast<const float2*>(smem + p.aux_off) +

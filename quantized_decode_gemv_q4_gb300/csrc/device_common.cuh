@@ -131,12 +131,6 @@ __device__ __forceinline__ float lds32f(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
-    uint32_t r;
-    // (a & mask) | orv
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));
-    return r;
-}
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
@@ -151,46 +145,7 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(
 // 4i+jj of sub-block 2c+1 (offset by 16*h inside the sub-block). Either way the 8 codes of a word land at
 // these bit positions p after the word and a copy shifted right by 12 are masked:
 //   low  jj=0..3: p = 0, 8, 16, 12      high jj=0..3: p = 4, 12, 8, 16
-constexpr int kPosLo[4] = {0, 8, 16, 12};
-constexpr int kPosHi[4] = {4, 12, 8, 16};
-constexpr uint32_t kOne = 0x3F800000u;
-
-// Scale factor 2^(23-p) applied to the staged input element for (half, jj).
-__host__ __device__ constexpr float pos_scale(int hi, int jj) {
-    return (float)(1u << (23 - (hi ? (jj == 0 ? 4 : jj == 1 ? 12 : jj == 2 ? 8 : 16)
-                                   : (jj == 0 ? 0 : jj == 1 ? 8 : jj == 2 ? 16 : 12))));
-}
-
-// The eight decoded values of one word as four float2 pairs, each already biased:
-//   lo01 = (lo jj0, lo jj1), lo23 = (lo jj2, lo jj3), hi01, hi23.
-struct Word8 {
-    float2 lo01, lo23, hi01, hi23;
-};
-
-template <int BIAS>
-__device__ __forceinline__ Word8 decode_word(uint32_t w) {
-    const uint32_t s = w >> 12;
-    float2 lo01 = make_float2(__uint_as_float(lop3_and_or(w, 0x0000000Fu, kOne)),
-                              __uint_as_float(lop3_and_or(w, 0x00000F00u, kOne)));
-    float2 lo23 = make_float2(__uint_as_float(lop3_and_or(w, 0x000F0000u, kOne)),
-                              __uint_as_float(lop3_and_or(s, 0x0000F000u, kOne)));
-    float2 hi01 = make_float2(__uint_as_float(lop3_and_or(w, 0x000000F0u, kOne)),
-                              __uint_as_float(lop3_and_or(w, 0x0000F000u, kOne)));
-    float2 hi23 = make_float2(__uint_as_float(lop3_and_or(s, 0x00000F00u, kOne)),
-                              __uint_as_float(lop3_and_or(s, 0x000F0000u, kOne)));
-    // bias pairs, constant-folded
-    const float2 b_lo01 = make_float2(-(1.0f + (float)BIAS * 0x1p-23f), -(1.0f + (float)BIAS * 0x1p-15f));
-    const float2 b_lo23 = make_float2(-(1.0f + (float)BIAS * 0x1p-7f), -(1.0f + (float)BIAS * 0x1p-11f));
-    const float2 b_hi01 = make_float2(-(1.0f + (float)BIAS * 0x1p-19f), -(1.0f + (float)BIAS * 0x1p-11f));
-    const float2 b_hi23 = make_float2(-(1.0f + (float)BIAS * 0x1p-15f), -(1.0f + (float)BIAS * 0x1p-7f));
-    Word8 r;
-    r.lo01 = fadd2(lo01, b_lo01);
-    r.lo23 = fadd2(lo23, b_lo23);
-    r.hi01 = fadd2(hi01, b_hi01);
-    r.hi23 = fadd2(hi23, b_hi23);
-    return r;
-}
-
+//
 // ------------------------------------------------------------------------------------------------
 // Bias-free nibble decode (subnormal codes) and block-scaled staging
 // ------------------------------------------------------------------------------------------------
@@ -205,20 +160,6 @@ __device__ __forceinline__ Word8 decode_word(uint32_t w) {
 // format's -8 offset, and the row accumulates d * t.
 // float4 loads each thread issues back to back while staging the input, before it uses any of them.
 constexpr int kStageU = 8;
-// Whole 32-element blocks (eight float4 each) a thread loads back to back while staging a planar-Q4 input.
-constexpr int kStageB = 2;
-
-// Sum and largest magnitude of one 32-element block held by one thread as eight float4 (fixed tree).
-__device__ __forceinline__ void block_sum_max(const float4 (&v)[8], float& sum, float& mx) {
-    float s[8], m[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        s[q] = (v[q].x + v[q].y) + (v[q].z + v[q].w);
-        m[q] = fmaxf(fmaxf(fabsf(v[q].x), fabsf(v[q].y)), fmaxf(fabsf(v[q].z), fabsf(v[q].w)));
-    }
-    sum = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-    mx = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
 
 struct Word8s {
     float2 lo01, lo23, hi01, hi23;  // (lo jj0, lo jj1), (lo jj2, lo jj3), (hi jj0, hi jj1), (hi jj2, hi jj3)
@@ -244,17 +185,6 @@ __device__ __forceinline__ int block_exponent(float m) {
     const int ef = (int)((__float_as_uint(m) >> 23) & 0xFFu);
     if (ef == 255) return 128;
     return max(ef - 126, -100);
-}
-
-// x * 2^(127-p-e) for the code position p of (half, jj), in two exact power-of-two steps (the exponent can
-// reach 227).
-__device__ __forceinline__ float stage_scaled(float x, int hi, uint32_t jj, int e) {
-    constexpr uint32_t lo_tab = 0u | (8u << 5) | (16u << 10) | (12u << 15);
-    constexpr uint32_t hi_tab = 4u | (12u << 5) | (8u << 10) | (16u << 15);
-    const int p = (int)(((hi ? hi_tab : lo_tab) >> (5u * jj)) & 31u);
-    const int k = 127 - p - e;
-    const int k1 = k >> 1;
-    return (x * pow2i(k1)) * pow2i(k - k1);
 }
 
 // Block factor 2^(22+e); +inf once that passes the float range (blocks with an element of magnitude 2^105
@@ -295,18 +225,6 @@ __device__ __forceinline__ Stage4 stage_block4(float4 a, float4 b, int hi) {
     return st;
 }
 
-
-// Sum and largest magnitude of 32 consecutive elements held as one float4 by each of 8 aligned lanes; every
-// lane of the group gets both (fixed summation tree).
-__device__ __forceinline__ void block8_sum_max(const float4& v, float& sum, float& mx) {
-    sum = (v.x + v.y) + (v.z + v.w);
-    mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-    for (int off = 4; off >= 1; off >>= 1) {
-        sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-}
 
 // Chunk-major staged input: float[ceil(U/32)][V][8 quads][32 unit lanes][4] for V vectors of U units. A
 // lane that always works on units u = 32c + lane finds every quad of every vector at one base register plus

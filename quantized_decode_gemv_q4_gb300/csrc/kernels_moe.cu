@@ -389,45 +389,40 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     for (int k = 0; k < D - 1; ++k) issue();
 
     if constexpr (!PURE) {
-        // Stage the T tokens block by block (each thread whole 32-element blocks, loads issued ahead).
+        // Stage the T tokens: four lanes per 32-element block, lane t of the group holding quads 2t and 2t+1
+        // (block sum and largest magnitude by two group shuffles); the loop covers whole warps so the
+        // shuffles always see 32 lanes.
         const int nb_all = p.T * U;
-        for (int base = threadIdx.x; base < nb_all; base += kThreads * kStageB) {
-            float4 xv[kStageB][8];
-#pragma unroll
-            for (int j = 0; j < kStageB; ++j) {
-                const int blk = base + j * kThreads;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    xv[j][q] = blk < nb_all ? __ldg(reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + q)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < kStageB; ++j) {
-                const int blk = base + j * kThreads;
-                if (blk < nb_all) {
-                    const int v = blk / U;
-                    const int u = blk - v * U;
-                    float bsum, bmax;
-                    block_sum_max(xv[j], bsum, bmax);
-                    const int e = block_exponent(bmax);
-                    // XG layout: [group of 32 blocks][token][quad][block in group]; otherwise [token][quad][block]
-                    // (16 bytes each): the lanes of a warp read consecutive 16-byte pieces either way
-                    const int grp32 = u >> 5, ul = u & 31;
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        const int hi = q8 >> 2;
-                        const uint32_t a = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q8) * 32 + ul) * 16
-                                                              : ((v * 8 + q8) * U + u) * 16);
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                     "f"(stage_scaled(xv[j][q8].x, hi, 0, e)), "f"(stage_scaled(xv[j][q8].y, hi, 1, e)),
-                                     "f"(stage_scaled(xv[j][q8].z, hi, 2, e)), "f"(stage_scaled(xv[j][q8].w, hi, 3, e))
-                                     : "memory");
-                    }
+        const int t4 = lane & 3;
+        const int nthr = (nb_all * 4 + 31) & ~31;
+        for (int thr = threadIdx.x; thr < nthr; thr += kThreads) {
+            const int blk = thr >> 2;
+            const bool in = blk < nb_all;
+            const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * t4;
+            const float4 xa = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 xb = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const Stage4 st = stage_block4(xa, xb, t4 >> 1);
+            if (in) {
+                const int v = blk / U;
+                const int u = blk - v * U;
+                // XG layout: [group of 32 blocks][token][quad][block in group]; otherwise [token][quad][block]
+                // (16 bytes each): the lanes of a warp read consecutive 16-byte pieces either way
+                const int grp32 = u >> 5, ul = u & 31;
+                const int q0 = 2 * t4;
+                const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * 32 + ul) * 16
+                                                       : ((v * 8 + q0) * U + u) * 16);
+                const uint32_t qstep = XG ? 512u : (uint32_t)U * 16u;
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
+                             "f"(st.a.z), "f"(st.a.w)
+                             : "memory");
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x), "f"(st.b.y),
+                             "f"(st.b.z), "f"(st.b.w)
+                             : "memory");
+                if (t4 == 0)
                     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
-                                                                                            : v * U + u) * 8)),
-                                 "f"(block_factor(e)), "f"(-8.0f * bsum)
+                                                                                                : v * U + u) * 8)),
+                                 "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
                                  : "memory");
-                }
             }
         }
     }

@@ -293,35 +293,55 @@ class Suite:
                 c1=(cu(c1["qs"]), cu(c1["d"])), c2=cu(c2["w"]), c3=(cu(c3["w_gate"]), cu(c3["w_up"])),
                 c4=[(cu(c4["qs"]), cu(c4["d"])) for _ in range(4)],  # one copy per batch width: each call cold
                 c5=(cu(c5["qs_gate"]), cu(c5["d_gate"]), cu(c5["qs_up"]), cu(c5["d_up"]))))
-        # per-step activations (device) and outputs
-        self.x1 = cu(c1["x"][0])
-        self.x2, self.g2 = cu(c2["x"]), cu(c2["gamma"])
-        self.x3, self.g3 = cu(c3["x"]), cu(c3["gamma"])
-        self.X4 = cu(c4["x"])
-        self.x5, self.ids5 = cu(c5["x"]), cu(c5["ids"])
-        f32 = dict(dtype=torch.float32, device=dev)
-        self.y1 = torch.empty(256, **f32)
-        self.y2 = torch.empty(3584, **f32)
-        self.y3g, self.y3u = torch.empty(18944, **f32), torch.empty(18944, **f32)
-        self.Y4 = [torch.empty(M, 14336, **f32) for M in (1, 2, 4, 8)]
-        self.y5g, self.y5u = torch.empty(8, 8, 1408, **f32), torch.empty(8, 8, 1408, **f32)
+        # Per-step activations and outputs, each set packed into one device buffer (256-byte aligned views) so
+        # that a step's inputs arrive by one copy and its outputs leave by one copy.
+        self.in_buf, (self.x1, self.x2, self.g2, self.x3, self.g3, self.X4, self.x5, self.ids5) = packed(
+            [c1["x"][0], c2["x"], c2["gamma"], c3["x"], c3["gamma"], c4["x"], c5["x"], c5["ids"]], dev)
+        f32 = np.float32
+        self.out_buf, outs = packed([np.zeros(256, f32), np.zeros(3584, f32), np.zeros(18944, f32),
+                                     np.zeros(18944, f32)] + [np.zeros((M, 14336), f32) for M in (1, 2, 4, 8)] +
+                                    [np.zeros((8, 8, 1408), f32), np.zeros((8, 8, 1408), f32)], dev)
+        self.y1, self.y2, self.y3g, self.y3u = outs[:4]
+        self.Y4 = outs[4:8]
+        self.y5g, self.y5u = outs[8:]
 
-    def calls(self, s):
-        """The step's calls on replica set s, as closures in launch order."""
+    def calls(self, s, stream=None):
+        """The step's calls on replica set s, as closures in launch order (on `stream`, else the current one)."""
         import quantized_decode_gemv_q4_gb300 as q4
 
         w = self.sets[s]
         c2eps = float(self.inputs[1]["eps"])
         c3eps = float(self.inputs[2]["eps"])
+        st = stream
         out = [
-            lambda: q4.q4_gemv(self.y1, w["c1"][0], w["c1"][1], self.x1),
-            lambda: q4.fused_rmsnorm_q4k_gemv(self.y2, w["c2"], self.x2, self.g2, c2eps),
-            lambda: q4.fused_gateup_q4k_gemv(self.y3g, self.y3u, w["c3"][0], w["c3"][1], self.x3, self.g3, c3eps),
+            lambda: q4.q4_gemv(self.y1, w["c1"][0], w["c1"][1], self.x1, stream=st),
+            lambda: q4.fused_rmsnorm_q4k_gemv(self.y2, w["c2"], self.x2, self.g2, c2eps, stream=st),
+            lambda: q4.fused_gateup_q4k_gemv(self.y3g, self.y3u, w["c3"][0], w["c3"][1], self.x3, self.g3, c3eps,
+                                             stream=st),
         ]
         for i, M in enumerate((1, 2, 4, 8)):
-            out.append(lambda i=i, M=M: q4.q4_gemv_batched(self.Y4[i], w["c4"][i][0], w["c4"][i][1], self.X4[:M]))
-        out.append(lambda: q4.moe_q4_gemv(self.y5g, self.y5u, *w["c5"], self.x5, self.ids5, 64))
+            out.append(lambda i=i, M=M: q4.q4_gemv_batched(self.Y4[i], w["c4"][i][0], w["c4"][i][1], self.X4[:M],
+                                                           stream=st))
+        out.append(lambda: q4.moe_q4_gemv(self.y5g, self.y5u, *w["c5"], self.x5, self.ids5, 64, stream=st))
         return out
+
+
+def packed(arrays, dev):
+    """One device byte buffer holding the given host arrays at 256-byte aligned offsets, and typed views of it
+    (in order) that start out holding the arrays' values."""
+    import torch
+
+    offs, n = [], 0
+    for a in arrays:
+        offs.append(n)
+        n += (a.nbytes + 255) // 256 * 256
+    host = np.zeros(n, np.uint8)
+    for a, o in zip(arrays, offs):
+        host[o:o + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).ravel()
+    buf = torch.from_numpy(host).to(dev)
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32}
+    views = [buf[o:o + a.nbytes].view(tdt[a.dtype]).view(a.shape) for a, o in zip(arrays, offs)]
+    return buf, views
 
 
 def capture(fns, stream):
@@ -561,31 +581,26 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
 
 
 def run_e2e(suite, inputs, stream, steps, table):
-    """Each step: copy the step's activations (and expert ids) from pinned host memory, make the eight calls
-    through the Python binding, read every output back to pinned host memory, wait for it."""
+    """Each step: copy the step's activations (and expert ids) from pinned host memory in one copy, make the
+    eight calls through the Python binding, read every output back to pinned host memory in one copy, wait."""
     import torch
 
     import quantized_decode_gemv_q4_gb300 as q4
 
-    c1, c2, c3, c4, c5 = inputs
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_in = [pin(c1["x"][0]), pin(c2["x"]), pin(c2["gamma"]), pin(c3["x"]), pin(c3["gamma"]), pin(c4["x"]),
-            pin(c5["x"]), pin(c5["ids"])]
-    d_in = [suite.x1, suite.x2, suite.g2, suite.x3, suite.g3, suite.X4, suite.x5, suite.ids5]
-    d_out = [suite.y1, suite.y2, suite.y3g, suite.y3u, *suite.Y4, suite.y5g, suite.y5u]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # the step's activations and ids in pinned host memory, laid out like the suite's packed input buffer
+    h_in = suite.in_buf.cpu().pin_memory()
+    h_out = torch.empty(suite.out_buf.shape, dtype=suite.out_buf.dtype).pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
     step_bytes = sum(t[1] for t in table)
+    calls = [suite.calls(s, stream) for s in range(len(suite.sets))]
 
     def step(i):
         with torch.cuda.stream(stream):
-            for d, h in zip(d_in, h_in):
-                d.copy_(h, non_blocking=True)
-            for fn in suite.calls(i % len(suite.sets)):
+            suite.in_buf.copy_(h_in, non_blocking=True)
+            for fn in calls[i % len(calls)]:
                 fn()
-            for h, d in zip(h_out, d_out):
-                h.copy_(d, non_blocking=True)
+            h_out.copy_(suite.out_buf, non_blocking=True)
         stream.synchronize()
 
     for i in range(5):
@@ -597,7 +612,7 @@ def run_e2e(suite, inputs, stream, steps, table):
     assert q4.q4_device_faults() == 0
     return {"value": round(step_bytes * steps / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
-            "path": "python binding, eager launches, pinned host copies, one host sync per step"}
+            "path": "python binding, eager launches, one pinned host copy in and one out, one host sync per step"}
 
 
 def cpu_baseline(inputs):

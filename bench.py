@@ -33,6 +33,9 @@ L2_BYTES = 129 * 2**20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+# The one metric both arms report (the reference arm's "time" is its host time for the same weight bytes).
+METRIC = "effective weight GB/s over the decode GEMV suite (weight bytes read / time)"
+
 KERNEL_SOURCES = ["device_common.cuh", "launch.h", "q4_dense.cuh", "kernels_q4.cu", "kernels_q4_v2_4.cu",
                   "kernels_q4_v5_8.cu", "kernels_q4_v9_16.cu", "kernels_q4k.cu", "kernels_q4k_rows.cu",
                   "kernels_q4k_batched.cu", "kernels_moe.cu", "kernels_router.cu"]
@@ -263,7 +266,7 @@ def run_reference(args):
     sample = (f"each step: the suite on the first {frac:.5f} of every matrix's rows (MoE: of every expert's rows), "
               "sized so that warm-up plus timed steps take about 90 s")
     line = {
-        "impl": "reference", "metric": "effective weight GB/s over the decode GEMV suite", "value": value,
+        "impl": "reference", "metric": METRIC, "value": value,
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": WORKLOAD_NAME, "sample": sample},
@@ -470,7 +473,7 @@ def run_gpu(args):
 
     if rank == 0:
         line = {
-            "metric": "effective weight GB/s over the decode GEMV suite (weight bytes read / device time)",
+            "metric": METRIC,
             "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tmax / args.steps * 1e3, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 (4-bit weights, fp32 inputs and accumulation)",

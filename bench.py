@@ -33,8 +33,9 @@ L2_BYTES = 129 * 2**20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-# The one metric both arms report (the reference arm's "time" is its host time for the same weight bytes).
-METRIC = "effective weight GB/s over the decode GEMV suite (weight bytes read / time)"
+# The one metric both arms report: `value` is the suite's weight bytes over its time (the reference arm's time is
+# its host time for the same bytes); `per_call` holds each call's GB/s, fraction of the HBM peak and us.
+METRIC = "effective weight GB/s per GEMV call and % of GB300 HBM peak; \u00b5s/call"
 
 KERNEL_SOURCES = ["device_common.cuh", "launch.h", "q4_dense.cuh", "kernels_q4.cu", "kernels_q4_v2_4.cu",
                   "kernels_q4_v5_8.cu", "kernels_q4_v9_16.cu", "kernels_q4k.cu", "kernels_q4k_rows.cu",

@@ -8,46 +8,13 @@
 namespace q4 {
 namespace dense {
 
-namespace {
-
-// Developer override of the single-vector plan, read once from Q4GEMV_Q4_V1="variant,upl_max,depth"
-// (variant 12: 16 warps x 2 rows; 22: the same with two accumulation chains; 11: 16 warps x 1 row;
-// 8: 8 warps x 4 rows, input in registers). Used for tuning sweeps; the default comes from such sweeps.
-struct V1Plan {
-    int variant = 12, upl_max = 4, depth = 2;
-};
-V1Plan v1_plan() {
-    static V1Plan o;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_Q4_V1");
-        if (e) sscanf(e, "%d,%d,%d", &o.variant, &o.upl_max, &o.depth);
-    });
-    return o;
-}
-
-}  // namespace
-
-// One vector: 16 warps x 2-row slots of half rows (64 blocks) in a ring of depth 5, so about 150 KB per SM
-// stay in flight while the warps compute; longer rows stream in 64-block chunks too.
+// One vector: 16 warps x 2 rows per lane, whole rows per stage up to K = 4096 (4 units per lane; longer rows in
+// 128-block chunks), ring depth 2 (3 on request through Q4GEMV_Q4_DEPTH). Measured slower at 14336x4096:
+// 16 warps x 1 row, 24 warps x 1 row, 10-14 warps x 2 rows, 8 warps x 4 rows with the input in registers,
+// two accumulation chains per row, rings of depth 3 to 8.
 cudaError_t gemv_v1(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int N,
                     int K, cudaStream_t s) {
-    const V1Plan pl = v1_plan();
-    cudaError_t e = cudaErrorNotSupported;
-    switch (pl.variant) {
-        case 22: e = launch<1, 2, 16, 8, false, false, 2>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 11: e = launch<1, 1, 16, 8, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 14: e = launch<1, 2, 14, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 13: e = launch<1, 2, 12, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 10: e = launch<1, 2, 10, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 24: e = launch<1, 1, 24, 4, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s); break;
-        case 8:
-            if (K / 32 <= 128) e = launch<1, 4, 8, 2, true, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            break;
-        default: break;
-    }
-    if (e == cudaErrorNotSupported) e = launch<1, 2, 16, 8, false, false>(di, Y, qs, d, X, N, K, pl.depth, pl.upl_max, s);
-    return e;
+    return launch<1, 2, 16, 3, false>(di, Y, qs, d, X, N, K, 2, 4, s);
 }
 
 }  // namespace dense
@@ -64,14 +31,13 @@ cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const
     return cudaErrorInvalidValue;
 }
 
-// The same streaming as the single-vector plan (16 warps, 2-row slots of up to 64 blocks, ring depth 5), no
+// The same streaming as the single-vector plan (16 warps x 2 rows, whole rows per stage, ring depth 2), no
 // math.
 cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s) {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
-    const dense::V1Plan pl = dense::v1_plan();
-    return dense::launch<1, 2, 16, 8, false, true>(di, sink, qs, d, nullptr, N, K, pl.depth, pl.upl_max, s);
+    return dense::launch<1, 2, 16, 3, true>(di, sink, qs, d, nullptr, N, K, 2, 4, s);
 }
 
 namespace {

@@ -9,11 +9,11 @@
 // Kernel shape (one persistent CTA of W warps per SM):
 //  * the V input vectors are staged once per CTA in shared memory, block by block: each element is
 //    pre-scaled for the bit position of its code and its block's exponent bound, and beside each block sit
-//    its factor 2^(22+e) and -8 times its sum (device_common.cuh, bias-free decode). With XREG (V = 1) every
-//    lane then copies the quads of its own units into registers, so the main loop reads no staged input;
-//  * every warp owns a ring of D shared-memory slots filled by warp-cooperative cp.async copies; a slot holds
-//    R consecutive rows x CB = 32*UPL blocks (quants, then scales), so each weight byte is read from HBM once
-//    and all V vectors use it. Whole rows of exactly CB blocks travel as one contiguous copy;
+//    its factor 2^(22+e) and -8 times its sum (device_common.cuh, bias-free decode);
+//  * every warp owns a ring of D shared-memory slots; a slot holds R consecutive rows x CB = 32*UPL blocks
+//    (quants, then scales), so each weight byte is read from HBM once and all V vectors use it. Whole rows of
+//    exactly CB blocks travel as two bulk copies (quants, scales) issued by lane 0 on the slot's mbarrier;
+//    chunks of longer rows by warp-cooperative 16-byte cp.async;
 //  * lane l handles units l, l+32, ... of every row in the slot, in increasing order whatever CB is, so
 //    the per-row summation order depends only on K: batched rows equal single-vector calls bit for bit;
 //  * per 32-bit word: one shift and eight ANDs turn the codes into floats, and four packed fp32x2 FMAs per
@@ -58,10 +58,8 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-template <int V, int R, int W, int D, int UPL, bool XREG, bool PURE, int NCH>
+template <int V, int R, int W, int D, int UPL, bool PURE>
 __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
-    static_assert(NCH == 1 || NCH == 2, "one or two accumulation chains per row and vector");
-    static_assert(!XREG || V == 1, "register-resident input holds one vector");
     constexpr int CB = 32 * UPL;
     constexpr uint32_t QROW = CB * 16u;
     constexpr uint32_t QBYTES = R * QROW;
@@ -193,23 +191,11 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     }
     __syncthreads();
 
-    // Register-resident input (V = 1, whole rows in one chunk): the quads and block pairs of this lane's
-    // units. Quads of units past the row end are never used.
     // Plain pointers into the shared array (not asm address operands), so that the unit offsets below fold
     // into the loads' immediates.
     const float4* const xs_p = reinterpret_cast<const float4*>(smem + p.xs_off) + lane;
     const float2* const aux_p = reinterpret_cast<const float2*>(smem + p.aux_off) + lane;
     const uint8_t* const ring_p = smem + p.slots_off + (size_t)warp * (D * SLOT);
-    float4 xr[XREG ? UPL : 1][8];
-    float2 ar[XREG ? UPL : 1];
-    if constexpr (XREG) {
-#pragma unroll
-        for (int it = 0; it < UPL; ++it) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) xr[it][q] = xs_p[it * 256 + q * 32];
-            ar[it] = aux_p[it * 32];
-        }
-    }
 
     float tot[R][V];
     uint32_t fold[R];
@@ -257,9 +243,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
             } else {
-                // NCH = 1: one fp32x2 chain per row and vector; NCH = 2: low and high codes in separate chains
-                // (shorter dependency chains), added at the end of the unit.
-                float2 acc[R][V][NCH];
+                // one fp32x2 chain per row and vector
+                float2 acc[R][V];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     Word8s d8[R];
@@ -268,45 +253,32 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                         d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        float4 xl, xh;
-                        if constexpr (XREG) {
-                            xl = xr[it][i];
-                            xh = xr[it][4 + i];
-                        } else {
-                            const float4* const xa = xb + (it * V + v) * 256 + i * 32;
-                            xl = xa[0];
-                            xh = xa[128];
-                        }
+                        const float4* const xa = xb + (it * V + v) * 256 + i * 32;
+                        const float4 xl = xa[0];
+                        const float4 xh = xa[128];
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][v][0];
+                            float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][v];
                             a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
                             a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
-                            float2 b = NCH == 1 ? a : (i == 0 ? make_float2(0.f, 0.f) : acc[r][v][NCH - 1]);
-                            b = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), b);
-                            b = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), b);
-                            if constexpr (NCH == 2) acc[r][v][0] = a;
-                            acc[r][v][NCH - 1] = b;
+                            a = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), a);
+                            a = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), a);
+                            acc[r][v] = a;
                         }
                     }
                 }
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    float2 fa;
-                    if constexpr (XREG)
-                        fa = ar[it];
-                    else
-                        fa = ab[(it * V + v) * 32];
+                    const float2 fa = ab[(it * V + v) * 32];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float2 sa = NCH == 1 ? acc[r][v][0] : fadd2(acc[r][v][0], acc[r][v][NCH - 1]);
-                        const float t = fmaf(sa.x + sa.y, fa.x, fa.y);
+                        const float t = fmaf(acc[r][v].x + acc[r][v].y, fa.x, fa.y);
                         tot[r][v] = fmaf(dsc[r], t, tot[r][v]);
                     }
                 }
             }
         };
-        if constexpr (XREG || R * V <= 2) {
+        if constexpr (R * V <= 2) {
             // short bodies: unrolled, so neighbouring units overlap; full chunks run unguarded
             if (nb == CB) {
 #pragma unroll
@@ -394,7 +366,7 @@ inline int depth_override(int d) {
     return o > 0 ? o : d;
 }
 
-template <int V, int R, int W, int D, int UPL, bool XREG, bool PURE, int NCH>
+template <int V, int R, int W, int D, int UPL, bool PURE>
 cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N,
                          int K, bool dcopy, cudaStream_t s) {
     constexpr int CB = 32 * UPL;
@@ -404,8 +376,7 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     const uint32_t barb = round_up_u((uint32_t)(W * D * 8 + 4), 128u);  // slot mbarriers and the error word
     const uint32_t smem = xsb + axb + barb + (uint32_t)(W * D) * slot_bytes<R, UPL>();
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
-    if (XREG && (int)nblk > CB) return cudaErrorNotSupported;
-    auto kern = q4_gemv_kernel<V, R, W, D, UPL, XREG, PURE, NCH>;
+    auto kern = q4_gemv_kernel<V, R, W, D, UPL, PURE>;
     static std::once_flag attr_once[64];
     cudaError_t err = cudaSuccess;
     std::call_once(attr_once[di.device & 63], [&] {
@@ -433,28 +404,27 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
 }
 
 // The deepest ring among the instantiated depths {2, 3, 4, 5, 6, 8} not above DMAX nor `want` that fits.
-template <int V, int R, int W, int DMAX, int UPL, bool XREG, bool PURE, int NCH>
+template <int V, int R, int W, int DMAX, int UPL, bool PURE>
 cudaError_t launch_upl(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N,
                        int K, bool dcopy, int want, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
 #define Q4_TRY_DEPTH(DD)                                                                              \
     if constexpr (DMAX >= DD)                                                                         \
         if (e == cudaErrorNotSupported && want >= DD)                                                 \
-            e = launch_fixed<V, R, W, DD, UPL, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, s);
+            e = launch_fixed<V, R, W, DD, UPL, PURE>(di, y, qs, d, x, N, K, dcopy, s);
     Q4_TRY_DEPTH(8)
     Q4_TRY_DEPTH(6)
     Q4_TRY_DEPTH(5)
     Q4_TRY_DEPTH(4)
     Q4_TRY_DEPTH(3)
 #undef Q4_TRY_DEPTH
-    if (e == cudaErrorNotSupported) e = launch_fixed<V, R, W, 2, UPL, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, s);
+    if (e == cudaErrorNotSupported) e = launch_fixed<V, R, W, 2, UPL, PURE>(di, y, qs, d, x, N, K, dcopy, s);
     return e;
 }
 
 // Units per lane: the whole row in one chunk up to min(K/32, 32*upl_max) blocks (UPL = 1, 2, 4), longer rows
-// in chunks of that size. With the input in shared memory, smaller chunks when the rings would not fit beside
-// it; register-resident input needs the whole row in one chunk.
-template <int V, int R, int W, int DMAX, bool XREG, bool PURE, int NCH = 1>
+// in chunks of that size; smaller chunks when the rings would not fit beside the staged input.
+template <int V, int R, int W, int DMAX, bool PURE>
 cudaError_t launch(const DeviceInfo& di, float* y, const uint8_t* qs, const uint16_t* d, const float* x, int N, int K,
                    int depth, int upl_max, cudaStream_t s) {
     const int nblk = K / 32;
@@ -462,11 +432,10 @@ cudaError_t launch(const DeviceInfo& di, float* y, const uint8_t* qs, const uint
     depth = std::min(depth_override(depth), DMAX);
     const int upl0 = std::min(nblk <= 32 ? 1 : nblk <= 64 ? 2 : 4, upl_max);
     cudaError_t e = cudaErrorNotSupported;
-    if (upl0 == 4) e = launch_upl<V, R, W, DMAX, 4, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
-    if (e == cudaErrorNotSupported && (upl0 == 2 || (!XREG && upl0 > 2)))
-        e = launch_upl<V, R, W, DMAX, 2, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
-    if (e == cudaErrorNotSupported && (upl0 == 1 || !XREG))
-        e = launch_upl<V, R, W, DMAX, 1, XREG, PURE, NCH>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    if (upl0 == 4) e = launch_upl<V, R, W, DMAX, 4, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    if (e == cudaErrorNotSupported && upl0 >= 2)
+        e = launch_upl<V, R, W, DMAX, 2, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
+    if (e == cudaErrorNotSupported) e = launch_upl<V, R, W, DMAX, 1, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
     return e;
 }
 

@@ -29,7 +29,7 @@ def run_router(qs, d, x, topk, normalize):
 
 
 @pytest.mark.parametrize("E,K,T,topk", [(64, 2048, 8, 8), (16, 256, 3, 4), (128, 4096, 1, 2), (7, 96, 5, 7),
-                                        (300, 1024, 2, 33)])
+                                        (300, 1024, 2, 33), (1, 256, 2, 1), (4096, 512, 2, 8)])
 @pytest.mark.parametrize("normalize", [True, False])
 def test_router_matches_oracle(E, K, T, topk, normalize, oracle_lib):
     rng = np.random.default_rng(E * 1000 + K + T)

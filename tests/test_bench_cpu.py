@@ -22,6 +22,27 @@ def test_reference_arm_prints_one_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["steps"] == 2 and line["warmup"] == 3
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert line["metric"] == bench.METRIC  # the GPU arm prints the same metric string
+
+
+def test_packed_views_are_aligned_and_hold_the_arrays():
+    """The per-step inputs and outputs live in one buffer each (one host copy per direction): every view starts
+    on a 256-byte boundary (the kernels want 16) and holds its array's values and type."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    arrays = [np.arange(7, dtype=np.float32), np.arange(6, dtype=np.int32).reshape(2, 3),
+              np.full((3, 5), 2.5, np.float32)]
+    buf, views = bench.packed(arrays, "cpu")
+    for a, v in zip(arrays, views):
+        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
+        assert tuple(v.shape) == a.shape and np.array_equal(v.numpy(), a)
+    assert buf.numel() == 3 * 256
 
 
 def test_warmup_below_three_is_refused():

@@ -265,11 +265,19 @@ void oracle_swiglu(const double *g, const double *u, int64_t n, double *y)
     for (int64_t i = 0; i < n; ++i) y[i] = oracle_silu(g[i]) * u[i];
 }
 
+/* Selection order of the top-K: a ranks above b when a > b, and a NaN ranks below every other value. */
+static int ranks_above(double a, double b)
+{
+    if (isnan(a)) return 0;
+    return isnan(b) || a > b;
+}
+
 /*
  * Top-K softmax of one row of E logits (given as float or double through `get`): ids[0..topk) are the
- * indices of the topk largest logits in descending order (ties: lower index first); weights[i] is the
- * softmax probability of ids[i] over all E logits, divided by the sum of the topk probabilities when
- * `normalize` is non-zero. Plain selection: topk passes over the logits.
+ * indices of the topk largest logits in descending order (ties, including two NaNs: lower index first; a NaN
+ * below every other value); weights[i] is the softmax probability of ids[i] over all E logits (NaN for every
+ * pick when any logit is NaN), divided by the sum of the topk probabilities when `normalize` is non-zero.
+ * Plain selection: topk passes over the logits.
  */
 static void topk_softmax_row(const double *lg, int64_t E, int64_t topk, int normalize, int32_t *ids, double *weights)
 {
@@ -285,7 +293,7 @@ static void topk_softmax_row(const double *lg, int64_t E, int64_t topk, int norm
             for (int64_t j = 0; j < i; ++j)
                 if (ids[j] == e) taken = 1;
             if (taken) continue;
-            if (best < 0 || lg[e] > lg[best]) best = e;
+            if (best < 0 || ranks_above(lg[e], lg[best])) best = e;
         }
         ids[i] = (int32_t)best;
         weights[i] = exp(lg[best] - mx) / z;

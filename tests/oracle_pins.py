@@ -370,6 +370,15 @@ def pin_topk_softmax(o):
     assert np.allclose(w[0], p[[1, 3, 4]], rtol=1e-15, atol=0)
     ids2, w2 = o.topk_softmax_f32(lg, 3, True)
     assert ids2.tolist() == [[1, 3, 4]] and np.allclose(w2[0], p[[1, 3, 4]] / p[[1, 3, 4]].sum(), rtol=1e-15)
+    # NaN ranks below every other value (-inf included), two NaNs tie to the lower index, -0 ties with +0, and a
+    # NaN anywhere makes every softmax weight NaN (worked by hand)
+    nan = np.float32(np.nan)
+    ids3, w3 = o.topk_softmax_f32(np.array([[nan, 1.0, -np.inf, 1.0, nan]], np.float32), 5, False)
+    assert ids3.tolist() == [[1, 3, 2, 0, 4]] and np.all(np.isnan(w3))
+    ids4, _ = o.topk_softmax_f32(np.array([[nan, 2.0, nan, -3.0]], np.float32), 2, True)
+    assert ids4.tolist() == [[1, 3]]
+    ids5, w5 = o.topk_softmax_f32(np.array([[-0.0, 0.0, -1.0]], np.float32), 2, False)
+    assert ids5.tolist() == [[0, 1]] and np.allclose(w5[0], np.exp([0.0, 0.0]) / (2 + np.exp(-1.0)), rtol=1e-15)
     rng = np.random.default_rng(31)
     for E, K in ((64, 8), (16, 2), (7, 7), (128, 1)):
         L = (rng.standard_normal((5, E)) * 3).astype(np.float32)

@@ -16,8 +16,10 @@ import oracle_pins
 MUTATIONS = [
     ("silu sign", "return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
     ("swiglu uses u twice", "y[i] = oracle_silu(g[i]) * u[i];", "y[i] = oracle_silu(u[i]) * u[i];"),
-    ("top-k ties to the higher index", "if (best < 0 || lg[e] > lg[best]) best = e;",
-     "if (best < 0 || lg[e] >= lg[best]) best = e;"),
+    ("top-k ties to the higher index", "return isnan(b) || a > b;", "return isnan(b) || a >= b;"),
+    ("top-k NaN ranked by plain comparison", "if (best < 0 || ranks_above(lg[e], lg[best])) best = e;",
+     "if (best < 0 || lg[e] > lg[best]) best = e;"),
+    ("top-k NaN ranked first", "    if (isnan(a)) return 0;", "    if (isnan(a)) return 1;"),
     ("top-k weights not renormalised", "for (int64_t i = 0; i < topk; ++i) weights[i] /= s;",
      "for (int64_t i = 0; i < topk; ++i) weights[i] /= 1.0;"),
     ("softmax over the top-k only", "weights[i] = exp(lg[best] - mx) / z;", "weights[i] = exp(lg[best] - mx);"),

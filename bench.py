@@ -5,7 +5,9 @@ One step is one call of every GEMV entry point on its workload:
   q4_gemv_batched 14336x4096 at M = 1, 2, 4 and 8, and moe_q4_gemv (64 experts x 1408x2048, 8 tokens x top-8).
 The metric is effective weight bandwidth: the weight bytes each call must read (for MoE, the distinct selected
 experts' bytes) divided by device time. Steps replay CUDA graphs over two replica sets of all weights, so each
-call reads weights that were last touched about 650 MB of traffic earlier (the L2 holds 129 MB).
+call reads weights that were last touched about 650 MB of traffic earlier (the L2 holds 129 MB). Per-call times
+(`per_call`) come from graphs of one call type back to back over weight copies of at least 3x the L2, with the
+spread of five batches, a launch-inclusive single-call time and the pure-read instrument of the same bytes.
 
 Prints one JSON line (rank 0). ``--impl reference`` times the plain-C fp64 oracle instead (host cores).
 """
@@ -429,30 +431,10 @@ def run_gpu(args):
     del plain
     q4.q4_set_launch_overlap(True)
 
-    # ---- per-call device time: each call type alone, back to back in one graph over the replica sets ---
-    reps = 8 * replicas
-    kt_us = np.zeros(n_calls)
-    for j in range(n_calls):
-        fns = [suite.calls(i % replicas)[j] for i in range(reps)]
-        g = capture(fns, stream)
-        with torch.cuda.stream(stream):
-            g.replay()
-        best = float("inf")
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record()
-                g.replay()
-                b.record()
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / reps * 1e3)
-        kt_us[j] = best
-        del g
+    # ---- per-call device time: each call type alone, back to back over weight copies of >= 3x the L2 ------
     peak, peak_kind = measured_peaks()
-    per_call = []
-    for (name, b, _), us in zip(table, kt_us):
-        per_call.append({"call": name, "us": round(float(us), 3), "weight_GBps": round(b / us / 1e3, 1),
-                         "frac_of_hbm_peak": round(b / us / 1e3 / peak, 4)})
+    per_call = measure_per_call(suite, inputs, table, stream, peak)
+    kt_us = np.array([pc["us"] for pc in per_call])
     dom = int(np.argmax(kt_us))
     traffic = committed_traffic(table[dom][2])
     achieved = table[dom][1] / kt_us[dom] / 1e3
@@ -461,7 +443,7 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes": table[dom][1], "us_per_launch": round(float(kt_us[dom]), 3)}
 
-    # ---- SURVEY NEXT rows, timed the same way but outside the headline step ------------------------------
+    # ---- the NEXT rows (router, SwiGLU forms, wider batches, launch chain), timed the same way ------
     next_rows = measure_next_rows(suite, inputs, stream, replicas, peak)
 
     # ---- end to end through the Python API with host buffers ---------------------------------------
@@ -480,8 +462,10 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "f32 (4-bit weights, fp32 inputs and accumulation)",
             "data": "synthetic (seeded generators; no trained weights)",
             "config": {"workload": WORKLOAD_NAME, "weight_bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2: 2 replica sets of all weights (846 MB), each call reads "
-                             "weights last touched ~650 MB of traffic earlier", "graph": "one CUDA graph per step",
+                       "l2": "inputs larger than L2: the step rotates 2 replica sets of all weights (846 MB), each "
+                             "call reads weights last touched ~650 MB of traffic earlier; per_call and next_rows "
+                             "rotate each call over weight copies of >= 3x the L2 (rotation_bytes)",
+                       "graph": "one CUDA graph per step",
                        "launch_overlap": "on (programmatic dependent launch: each call's first weight copies "
                                          "overlap the previous call's tail)",
                        "value_without_launch_overlap": round(value_plain, 1),
@@ -497,14 +481,31 @@ def run_gpu(args):
     return 0
 
 
-def _graph_us(fns, stream, reps=16, tries=5):
-    """Best per-launch device time of a graph of `reps` calls (fns rotated), after one replay."""
+def cold_copies(tensors, nbytes):
+    """Device copies of a weight set, enough that their bytes (`nbytes` read per call) reach 3x the L2: calls
+    rotated over them read weights no earlier call left in the L2. Each copy is a slice of one allocation per
+    tensor (contiguous, 256-byte aligned when the tensor's size is)."""
     import torch
 
+    k = max(2, int(np.ceil(3 * L2_BYTES / nbytes)))
+    stacks = []
+    for t in tensors:
+        s = torch.empty((k,) + tuple(t.shape), dtype=t.dtype, device=t.device)
+        s.copy_(t.unsqueeze(0).expand_as(s))
+        stacks.append(s)
+    return [tuple(s[i] for s in stacks) for i in range(k)], k
+
+
+def _graph_us(fns, stream, reps=None, tries=5):
+    """Per-launch device time of a CUDA graph of `reps` calls (fns rotated; default: each once, at least 16):
+    one replay discarded, then the best of `tries` timed replays and the spread (worst / best)."""
+    import torch
+
+    reps = reps or max(16, len(fns))
     g = capture([fns[i % len(fns)] for i in range(reps)], stream)
     with torch.cuda.stream(stream):
         g.replay()
-    best = float("inf")
+    times = []
     for _ in range(tries):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -512,13 +513,90 @@ def _graph_us(fns, stream, reps=16, tries=5):
             g.replay()
             b.record()
         b.synchronize()
-        best = min(best, a.elapsed_time(b) / reps * 1e3)
+        times.append(a.elapsed_time(b) / reps * 1e3)
     del g
-    return best
+    return min(times), max(times) / min(times)
+
+
+def _single_us(fn, stream, n=21):
+    """Launch-inclusive time of one call (events around one eager call, idle device before it): median of n."""
+    import torch
+
+    ts = []
+    for _ in range(n):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            fn()
+            b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(ts))
+
+
+def _entry(name, nbytes, us, spread, k, peak, **extra):
+    e = {"call": name, "us": round(us, 3), "weight_GBps": round(nbytes / us / 1e3, 1),
+         "frac_of_hbm_peak": round(nbytes / us / 1e3 / peak, 4), "spread": round(spread, 3),
+         "rotation_bytes": int(k * nbytes), "copies": k}
+    e.update(extra)
+    return e
+
+
+def measure_per_call(suite, inputs, table, stream, peak):
+    """Each suite call alone, back to back in one CUDA graph over weight copies whose bytes reach 3x the L2, so
+    every call streams its weights from HBM; the pure-read instrument of the same bytes beside it."""
+    import torch
+
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    w = suite.sets[0]
+    c2eps = float(inputs[1]["eps"])
+    c3eps = float(inputs[2]["eps"])
+    out = []
+
+    def one(j, fns, k, pure=None, pure_per_call=1):
+        us, spread = _graph_us(fns, stream)
+        single = _single_us(fns[0], stream)
+        extra = {"single_call_us": round(single, 3)}
+        if pure is not None:
+            pus, pspread = _graph_us(pure, stream)
+            pus *= pure_per_call  # instrument launches that read the call's bytes
+            extra["pure_read_us"] = round(pus, 3)
+            extra["pure_read_frac_of_hbm_peak"] = round(table[j][1] / pus / 1e3 / peak, 4)
+            extra["kernel_over_pure_read"] = round(us / pus, 3)
+        out.append(_entry(table[j][0], table[j][1], us, spread, k, peak, **extra))
+
+    cp, k = cold_copies(w["c1"], table[0][1])
+    one(0, [lambda c=c: q4.q4_gemv(suite.y1, c[0], c[1], suite.x1, stream=stream) for c in cp], k)
+    del cp
+    cp, k = cold_copies((w["c2"],), table[1][1])
+    one(1, [lambda c=c: q4.fused_rmsnorm_q4k_gemv(suite.y2, c[0], suite.x2, suite.g2, c2eps, stream=stream)
+            for c in cp], k)
+    del cp
+    cp, k = cold_copies(w["c3"], table[2][1])
+    one(2, [lambda c=c: q4.fused_gateup_q4k_gemv(suite.y3g, suite.y3u, c[0], c[1], suite.x3, suite.g3, c3eps,
+                                                 stream=stream) for c in cp], k,
+        pure=[lambda m=m: q4.q4k_pure_read(suite.y3g, m, stream=stream) for c in cp for m in c], pure_per_call=2)
+    del cp
+    cp, k = cold_copies(w["c4"][0], table[3][1])
+    for i, M in enumerate((1, 2, 4, 8)):
+        one(3 + i, [lambda c=c, i=i, M=M: q4.q4_gemv_batched(suite.Y4[i], c[0], c[1], suite.X4[:M], stream=stream)
+                    for c in cp], k,
+            pure=[lambda c=c: q4.q4_pure_read(suite.Y4[3][0], c[0], c[1], stream=stream) for c in cp] if M == 1 else None)
+    del cp
+    cp, k = cold_copies(w["c5"], table[7][1])
+    one(7, [lambda c=c: q4.moe_q4_gemv(suite.y5g, suite.y5u, *c, suite.x5, suite.ids5, 64, stream=stream)
+            for c in cp], k,
+        pure=[lambda c=c: q4.moe_q4_pure_read(suite.y5g, suite.y5u, *c, suite.ids5, 64, stream=stream) for c in cp])
+    del cp
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_next_rows(suite, inputs, stream, replicas, peak):
-    """The router, the SwiGLU forms and a dependent router -> MoE-SwiGLU chain on the suite's workloads."""
+    """The router, the SwiGLU forms, the wider batches and a dependent router -> MoE-SwiGLU chain, each over
+    weight copies of >= 3x the L2 like the suite's calls."""
     import torch
 
     import quantized_decode_gemv_q4_gb300 as q4
@@ -527,7 +605,7 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     rng = np.random.default_rng(7)
     E, K, T, topk = 64, 2048, 8, 8
-    rq, rd = synth.q4_weights(rng, E, K)  # router rows (73.7 KB: L2-resident, so latency-bound)
+    rq, rd = synth.q4_weights(rng, E, K)
     rq, rd = cu(rq), cu(rd)
     ids = torch.empty(T, topk, dtype=torch.int32, device=dev)
     wts = torch.empty(T, topk, device=dev)
@@ -535,52 +613,58 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
     ymo = torch.empty(T, topk, 1408, device=dev)
     c3eps = float(inputs[2]["eps"])
     out = {}
-    us = _graph_us([lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, topk, True)], stream)
-    out["moe_router_q4 e64 k2048 t8 top8"] = {"us": round(us, 3)}
+    rb = q4_bytes(E, K)
+    cp, k = cold_copies((rq, rd), rb)
+    us, sp = _graph_us([lambda c=c: q4.moe_router_q4(ids, wts, c[0], c[1], suite.x5, topk, True, stream=stream)
+                        for c in cp], stream)
+    out["moe_router_q4 e64 k2048 t8 top8"] = {"us": round(us, 3), "spread": round(sp, 3), "copies": k,
+                                              "note": "74 KB of router weights: launch-latency bound"}
+    del cp
     gb = 2 * q4k_bytes(18944, 3584)
-    us = _graph_us([lambda s=s: q4.fused_gateup_swiglu_q4k_gemv(ysw, suite.sets[s]["c3"][0], suite.sets[s]["c3"][1],
-                                                                suite.x3, suite.g3, c3eps) for s in range(replicas)],
-                   stream)
-    out["fused_gateup_swiglu_q4k_gemv 2x18944x3584"] = {"us": round(us, 3), "weight_GBps": round(gb / us / 1e3, 1),
-                                                        "frac_of_hbm_peak": round(gb / us / 1e3 / peak, 4)}
-    uniq = len(np.unique(inputs[4]["ids"]))
-    mb = 2 * uniq * q4_bytes(1408, 2048)
-    us = _graph_us([lambda s=s: q4.moe_q4_swiglu_gemv(ymo, *suite.sets[s]["c5"], suite.x5, suite.ids5, 64)
-                    for s in range(replicas)], stream)
-    out[f"moe_q4_swiglu_gemv e64 1408x2048 t8k8 ({uniq} experts)"] = {
-        "us": round(us, 3), "weight_GBps": round(mb / us / 1e3, 1), "frac_of_hbm_peak": round(mb / us / 1e3 / peak, 4)}
-    # unfused batched Q4_K on the gate matrix of the gate+up workload, and the planar batched GEMV at M = 16
+    cp, k = cold_copies(suite.sets[0]["c3"], gb)
+    us, sp = _graph_us([lambda c=c: q4.fused_gateup_swiglu_q4k_gemv(ysw, c[0], c[1], suite.x3, suite.g3, c3eps,
+                                                                    stream=stream) for c in cp], stream)
+    out["fused_gateup_swiglu_q4k_gemv 2x18944x3584"] = _entry("", gb, us, sp, k, peak)
+    # unfused batched Q4_K on the gate and up matrices of the same copies (12 matrices of 38 MB rotated)
     kb = q4k_bytes(18944, 3584)
     Xk = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 8, 3584))).to(dev)
+    mats = [m for c in cp for m in c]
     for M in (1, 8):
         Yk = torch.empty(M, 18944, device=dev)
-        mats = [suite.sets[s]["c3"][j] for s in range(replicas) for j in (0, 1)]  # 4 x 38 MB rotated
-        us = _graph_us([lambda m=m: q4.q4k_gemv_batched(Yk, m, Xk[:M]) for m in mats], stream)
-        out[f"q4k_gemv_batched 18944x3584 M={M}"] = {"us": round(us, 3), "weight_GBps": round(kb / us / 1e3, 1),
-                                                     "frac_of_hbm_peak": round(kb / us / 1e3 / peak, 4)}
-    qs16, d16 = synth.q4_weights(rng, 14336, 2048)
-    b16 = q4_bytes(14336, 2048)
-    n16 = int(np.ceil(3 * L2_BYTES / b16))  # copies rotated so every call reads cold weights (3x the L2)
-    w16 = [(cu(qs16), cu(d16)) for _ in range(n16)]
-    X16 = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 16, 2048))).to(dev)
-    Y16 = torch.empty(16, 14336, device=dev)
-    us = _graph_us([lambda i=i: q4.q4_gemv_batched(Y16, w16[i][0], w16[i][1], X16) for i in range(n16)], stream,
-                   reps=n16)
-    out["q4_gemv_batched 14336x2048 M=16"] = {"us": round(us, 3), "weight_GBps": round(b16 / us / 1e3, 1),
-                                              "fp32_TFLOPs": round(16 * 2 * 14336 * 2048 / us / 1e6, 2)}
-    del w16
+        us, sp = _graph_us([lambda m=m: q4.q4k_gemv_batched(Yk, m, Xk[:M], stream=stream) for m in mats], stream)
+        out[f"q4k_gemv_batched 18944x3584 M={M}"] = _entry("", kb, us, sp, len(mats) // 2, peak)
+    del cp, mats
+    uniq = len(np.unique(inputs[4]["ids"]))
+    mb = 2 * uniq * q4_bytes(1408, 2048)
+    cp, k = cold_copies(suite.sets[0]["c5"], mb)
+    us, sp = _graph_us([lambda c=c: q4.moe_q4_swiglu_gemv(ymo, *c, suite.x5, suite.ids5, 64, stream=stream)
+                        for c in cp], stream)
+    out[f"moe_q4_swiglu_gemv e64 1408x2048 t8k8 ({uniq} experts)"] = _entry("", mb, us, sp, k, peak)
     # dependent chain: the router's ids drive the MoE call on the device
     chain = []
     for ov in (True, False):
         q4.q4_set_launch_overlap(ov)
         fns = []
-        for s in range(replicas):
-            fns.append(lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, topk, True))
-            fns.append(lambda s=s: q4.moe_q4_swiglu_gemv(ymo, *suite.sets[s]["c5"], suite.x5, ids, 64))
-        chain.append(_graph_us(fns, stream, reps=16) * 2)
+        for c in cp:
+            fns.append(lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, topk, True, stream=stream))
+            fns.append(lambda c=c: q4.moe_q4_swiglu_gemv(ymo, *c, suite.x5, ids, 64, stream=stream))
+        chain.append(_graph_us(fns, stream)[0] * 2)
     q4.q4_set_launch_overlap(True)
     out["chain router -> moe_q4_swiglu_gemv (us per pair)"] = {"with_launch_overlap": round(chain[0], 3),
                                                                "without": round(chain[1], 3)}
+    del cp
+    qs16, d16 = synth.q4_weights(rng, 14336, 2048)
+    b16 = q4_bytes(14336, 2048)
+    cp, k = cold_copies((cu(qs16), cu(d16)), b16)
+    X16 = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 16, 2048))).to(dev)
+    Y16 = torch.empty(16, 14336, device=dev)
+    us, sp = _graph_us([lambda c=c: q4.q4_gemv_batched(Y16, c[0], c[1], X16, stream=stream) for c in cp], stream)
+    out["q4_gemv_batched 14336x2048 M=16"] = _entry("", b16, us, sp, k, peak,
+                                                    fp32_TFLOPs=round(16 * 2 * 14336 * 2048 / us / 1e6, 2))
+    del cp
+    for v in out.values():
+        v.pop("call", None)
+    torch.cuda.empty_cache()
     return out
 
 

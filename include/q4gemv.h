@@ -17,9 +17,13 @@
  *      Q4_EUNSUPPORTED the current device is not sm_103, or the staged input (M*K*4 bytes, T*K*4 for MoE)
  *                      does not fit in one CTA's shared memory next to the weight rings
  *    q4_last_error() describes the most recent refusal or failure of the calling thread.
- *  - Kernels never trap and contain no unbounded waits: each warp waits only for its own asynchronous copies
- *    (cp.async groups, or an mbarrier that its bulk copies complete). An mbarrier wait gives up after about
- *    4e9 SM cycles; the rows of every CTA in which that happened are then written as NaN.
+ *  - Kernels never trap and contain no unbounded spin: each warp waits only for its own asynchronous copies
+ *    (cp.async groups, or an mbarrier that its bulk or tensor copies complete). An mbarrier wait gives up after
+ *    q4_set_wait_limit's cycles (default 4e9, about two seconds); the warp whose wait ran out then issues no
+ *    further copies, stores NaN for every row it stores from then on (in the Q4_K row kernels, every row its CTA
+ *    stores from then on), records Q4_FAULT_WAIT_TIMEOUT, and before exiting waits (bounded by 4e9 cycles) for
+ *    the copies it had issued, so none lands in the shared memory of an exited CTA. Rows stored before the
+ *    timeout keep their values.
  *  - Inputs are fp32 vectors, outputs fp32. Weights are packed as described per format below; multi-byte
  *    fields are little-endian.
  *
@@ -66,7 +70,9 @@ enum {
 
 /* Fault bits reported by q4_device_faults. */
 enum {
-    Q4_FAULT_BAD_EXPERT = 4 /* moe_q4_gemv or moe_q4_pure_read saw an expert id outside [0, E) */
+    Q4_FAULT_BAD_EXPERT = 4,   /* moe_q4_gemv or moe_q4_pure_read saw an expert id outside [0, E) */
+    Q4_FAULT_WAIT_TIMEOUT = 8, /* a wait for a weight stage ran out of its cycle limit (rows written as NaN) */
+    Q4_FAULT_COPY_LOST = 16    /* even the final wait for a warp's issued copies ran out (not seen in practice) */
 };
 
 /*
@@ -112,7 +118,7 @@ int fused_rmsnorm_q4k_gemv(float *y, const uint8_t *w, const float *x, const flo
  * unfused Q4KGemvKernel); the batched contract of spark_model gemm_quant.rs, dense_gemv_batchm.
  *   Y float[M][N] (row-major), X float[M][K] (row-major, 16-byte aligned), w as fused_rmsnorm_q4k_gemv.
  *   1 <= M <= 8; N >= 1; K % 256 == 0. The M staged rows must fit in one CTA's shared memory beside the weight
- *   rings (M*K*4 + M*K/4 bytes: M = 8 up to K = 4096); larger inputs return Q4_EUNSUPPORTED. M = 1 runs the
+ *   rings (M*K*4 + M*K/2 bytes: M = 8 up to K = 4096); larger inputs return Q4_EUNSUPPORTED. M = 1 runs the
  *   kernel of fused_rmsnorm_q4k_gemv without the normalisation, so its summation order differs from M >= 2.
  */
 int q4k_gemv_batched(float *Y, const uint8_t *w, const float *X, int M, int N, int K, q4_stream_t stream);
@@ -223,6 +229,16 @@ const char *q4_last_error(void);
  */
 int q4_set_launch_overlap(int enable);
 int q4_get_launch_overlap(void);
+
+/*
+ * Limit, in SM cycles, of each kernel wait for a weight stage (no counterpart in the source pages). Process-wide,
+ * read at each launch (a CUDA graph keeps the value it captured); default 4000000000 (about two seconds). 0 makes
+ * every such wait give up at once without looking, which runs the timeout path (NaN rows, Q4_FAULT_WAIT_TIMEOUT)
+ * on copies that still land. q4_set_wait_limit returns Q4_OK, or Q4_EINVAL for a negative limit;
+ * q4_get_wait_limit returns the current limit.
+ */
+int q4_set_wait_limit(long long cycles);
+long long q4_get_wait_limit(void);
 
 /*
  * Synchronises the current device, then ORs the fault bits every kernel family recorded since the last

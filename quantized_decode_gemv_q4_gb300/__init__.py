@@ -25,11 +25,15 @@ __all__ = [
     "moe_q4_gemv", "q4k_gemv_batched", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "moe_router_q4", "q4_pure_read",
     "q4k_pure_read",
     "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
-    "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "FAULT_BAD_EXPERT",
+    "q4_device_faults", "q4_set_launch_overlap", "q4_get_launch_overlap", "q4_set_wait_limit", "q4_get_wait_limit",
+    "FAULT_BAD_EXPERT", "FAULT_WAIT_TIMEOUT", "FAULT_COPY_LOST", "DEFAULT_WAIT_LIMIT",
 ]
 
 Q4_OK, Q4_EINVAL, Q4_EALIGN, Q4_ECUDA, Q4_EUNSUPPORTED = 0, -1, -2, -3, -4
 FAULT_BAD_EXPERT = 4
+FAULT_WAIT_TIMEOUT = 8
+FAULT_COPY_LOST = 16
+DEFAULT_WAIT_LIMIT = 4_000_000_000
 _CODE_NAMES = {Q4_EINVAL: "EINVAL", Q4_EALIGN: "EALIGN", Q4_ECUDA: "ECUDA", Q4_EUNSUPPORTED: "EUNSUPPORTED"}
 
 
@@ -84,6 +88,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.q4_set_launch_overlap.restype = ctypes.c_int
         L.q4_get_launch_overlap.argtypes = []
         L.q4_get_launch_overlap.restype = ctypes.c_int
+        L.q4_set_wait_limit.argtypes = [ctypes.c_longlong]
+        L.q4_set_wait_limit.restype = ctypes.c_int
+        L.q4_get_wait_limit.argtypes = []
+        L.q4_get_wait_limit.restype = ctypes.c_longlong
         _lib = L
     return _lib
 
@@ -281,6 +289,17 @@ def q4_set_launch_overlap(enable: bool) -> None:
 
 def q4_get_launch_overlap() -> bool:
     return bool(load().q4_get_launch_overlap())
+
+
+def q4_set_wait_limit(cycles: int) -> None:
+    """Set the limit, in SM cycles, of each kernel wait for a weight stage (default DEFAULT_WAIT_LIMIT). A wait
+    that runs out makes its warp store NaN rows and record FAULT_WAIT_TIMEOUT; 0 makes every such wait give up at
+    once, which exercises that path."""
+    _check(load().q4_set_wait_limit(int(cycles)))
+
+
+def q4_get_wait_limit() -> int:
+    return int(load().q4_get_wait_limit())
 
 
 def q4_device_faults() -> int:

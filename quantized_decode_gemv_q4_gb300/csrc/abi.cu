@@ -95,9 +95,35 @@ int finish(const char* what, cudaError_t e) {
 
 namespace {
 std::atomic<int> g_launch_overlap{0};
+std::atomic<long long> g_wait_limit{4000000000LL};
 }  // namespace
 
 bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
+
+// The fault word every kernel family ORs its kFault* bits into (one per device that loads the library).
+static __device__ unsigned g_faults;
+
+unsigned* device_fault_word(int device) {
+    static unsigned* ptrs[64] = {};
+    static std::mutex mu;
+    if (device < 0 || device >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[device]) {
+        unsigned* p = nullptr;
+        if (cudaGetSymbolAddress((void**)&p, g_faults) != cudaSuccess) return nullptr;
+        ptrs[device] = p;
+    }
+    return ptrs[device];
+}
+
+static cudaError_t read_and_clear_faults(unsigned* out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_faults, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_faults, &zero, sizeof(unsigned));
+    return e;
+}
 
 cudaError_t current_device_info(DeviceInfo* out) {
     static DeviceInfo cache[64];
@@ -326,9 +352,18 @@ int q4_device_faults(unsigned* faults) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(what, e);
     unsigned f = 0;
-    if ((e = read_and_clear_fault_moe(&f)) != cudaSuccess) return cuda_fail(what, e);
-    *faults = f;
+    if ((e = read_and_clear_faults(&f)) != cudaSuccess) return cuda_fail(what, e);
+    *faults |= f;
     return finish(what, cudaSuccess);
 }
+
+int q4_set_wait_limit(long long cycles) {
+    if (cycles < 0) return fail(Q4_EINVAL, "q4_set_wait_limit: the limit must be >= 0 (got %lld)", cycles);
+    g_wait_limit.store(cycles, std::memory_order_relaxed);
+    g_last_error.clear();
+    return Q4_OK;
+}
+
+long long q4_get_wait_limit(void) { return g_wait_limit.load(std::memory_order_relaxed); }
 
 }  // extern "C"

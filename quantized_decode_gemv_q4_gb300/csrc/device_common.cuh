@@ -1,15 +1,14 @@
 // Device-side building blocks shared by the decode-GEMV kernels (sm_103a).
 //
-// * Weight streaming: each warp owns a ring of D shared-memory slots and fills them with warp-cooperative
-//   16-byte async copies (cp.async, one commit group per slot, consecutive lanes on consecutive 16 bytes).
-//   A warp waits only for its own groups (cp.async.wait_group), so there is no spin loop anywhere. On GB300
-//   this path streamed a 33 MB row-major weight matrix in 6.2 us against 7.4 us for 1-D bulk (TMA) copies
-//   of 8-16 KB, whose per-SM throughput capped near 4.4 TB/s in the same test.
-// * Nibble -> fp32: a 4-bit code that sits at bit p of a 32-bit word is turned into the float
-//   1 + q * 2^(p-23) by one LOP3 (mask the nibble, OR in the exponent of 1.0). Subtracting a per-position
-//   constant with the packed fp32x2 add is exact (Sterbenz), leaving (q - bias) * 2^(p-23). The input
-//   vector is staged in shared memory pre-multiplied by 2^(23-p) for the matching element, so the fp32x2
-//   FMA sees exactly (q - bias) * x and rounds once, as a plain fp32 FMA of the decoded weight would.
+// * Weight streaming: each warp owns a ring of shared-memory slots, filled by asynchronous bulk copies (TMA)
+//   that complete on one mbarrier per slot; a warp waits only for its own copies, and every wait is bounded.
+// * Nibble -> fp32 (bias-free decode): masking the 4-bit code that sits at bit p of a 32-bit word leaves the
+//   float q * 2^(p-149) exactly (a subnormal). The matching input element is staged pre-scaled by
+//   2^(127-p-e) (e bounds its 32-element block's exponent), so one packed fp32x2 FMA adds q * x * 2^(-22-e)
+//   with one rounding.
+// * The FMA chain of a 32-code unit (word_fma) is the one order every kernel uses, and the planar format's -8
+//   offset is removed with the same chain run on a unit of code 8 (q4_block_bias), so a block whose codes are
+//   all 8 (zero weights) contributes exactly zero.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -19,8 +18,14 @@ namespace q4 {
 
 // Fault bits recorded by kernels (read back by the host through the ABI).
 enum : unsigned {
-    kFaultBadExpert = 4u,  // an MoE expert id was outside [0, E)
+    kFaultBadExpert = 4u,    // an MoE expert id was outside [0, E)
+    kFaultWaitTimeout = 8u,  // a wait for a weight stage ran out of its cycle limit (the warp's later rows are NaN)
+    kFaultCopyLost = 16u,    // even the final drain wait for a warp's issued copies ran out (should never happen)
 };
+
+// Bound of the drain wait a warp makes before exit for copies it issued but no longer consumes (about two
+// seconds of SM clock); the per-stage limit is a kernel parameter (q4_set_wait_limit).
+constexpr long long kDrainCycles = 4000000000LL;
 
 // ------------------------------------------------------------------------------------------------
 // PTX wrappers
@@ -70,9 +75,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0u;
 }
-// Bound on one wait for a stage's copies (about two seconds of SM clock).
-constexpr long long kWaitCycles = 4000000000LL;
-
 // Wait for the completion of phase `parity` of an mbarrier, bounded by `max_cycles`; false if it ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long max_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -80,6 +82,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > max_cycles) return false;
     return true;
+}
+
+// The same wait by every lane of a warp, made warp-uniform: true only if every lane saw the phase complete.
+// A limit of 0 gives up at once without looking (it exercises the timeout path deterministically).
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, long long max_cycles) {
+    if (max_cycles <= 0) return false;
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, max_cycles)) != 0;
 }
 
 // Contiguous global -> shared bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned),
@@ -173,6 +182,29 @@ __device__ __forceinline__ Word8s decode_word_sub(uint32_t w) {
     r.hi01 = make_float2(__uint_as_float(w & 0x000000F0u), __uint_as_float(w & 0x0000F000u));
     r.hi23 = make_float2(__uint_as_float(s & 0x00000F00u), __uint_as_float(s & 0x000F0000u));
     return r;
+}
+
+// One 32-bit word of a unit against its staged quads: the low pairs (jj 0,1), (jj 2,3) then the high pairs, each
+// one packed FMA into the running (even, odd) pair. Every kernel accumulates a unit's four words in this order
+// (word 0 first, starting from zero), so equal codes and inputs give equal sums whatever the kernel.
+__device__ __forceinline__ float2 word_fma(const Word8s& d8, float4 xl, float4 xh, float2 a) {
+    a = ffma2(d8.lo01, make_float2(xl.x, xl.y), a);
+    a = ffma2(d8.lo23, make_float2(xl.z, xl.w), a);
+    a = ffma2(d8.hi01, make_float2(xh.x, xh.y), a);
+    a = ffma2(d8.hi23, make_float2(xh.z, xh.w), a);
+    return a;
+}
+
+// The block term of the planar format's -8 offset: -(A8 * 2^(22+e)) with A8 the unit chain of a block whose 32
+// codes are all 8, on the block's staged quads xq[8] (quad i: low codes of word i, quad 4+i: high codes) and
+// factor f = 2^(22+e). A block is then folded as t = fma(A, f, bias), which is exactly zero when its codes are
+// all 8 (A equals A8 bit for bit, and A8 * f is exact), and otherwise equals A * f - 8 * sum(x) up to rounding.
+__device__ __forceinline__ float q4_block_bias(const float4 (&xq)[8], float f) {
+    const Word8s c8 = decode_word_sub(0x88888888u);
+    float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a = word_fma(c8, xq[i], xq[4 + i], a);
+    return -((a.x + a.y) * f);
 }
 
 // 2^k for -126 <= k <= 127.

@@ -16,13 +16,16 @@
 //    control, and each selected expert's bytes are read once per call (once per group when more than kMaxC
 //    slots route to one expert);
 //  * all T input vectors are staged once per CTA, block by block, with the bias-free decode's per-block
-//    scaling (device_common.cuh): float4[K/32 blocks / 32][T][8 quads][32] and (2^(22+e), -8 * sum) pairs
-//    float2[K/32 / 32][T][32], so a lane's quads of a token sit at constant offsets from one base per stage;
+//    scaling (device_common.cuh): float4[K/32 blocks / 32][T][8 quads][32] and (2^(22+e), -8 offset term)
+//    pairs float2[K/32 / 32][T][32] (the offset term is the unit chain on codes of 8, q4_block_bias, so zero
+//    weights contribute exactly zero), and a lane's quads of a token sit at constant offsets from one base;
 //  * a job's slot count C (1..kMaxC) selects a compiled variant of the stage body, so each decoded code
-//    pair feeds exactly C packed FMAs; per block t = A * 2^(22+e) - 8 * sum(x), and the row accumulates
-//    d * t per routed slot;
+//    pair feeds exactly C packed FMAs in the common chain order (word_fma); per block t = A * 2^(22+e) + bias,
+//    and the row accumulates d * t per routed slot;
 //  * at the end of a row group the R*C totals are summed across the warp with a transposing shuffle
-//    reduction and stored to each slot's output rows.
+//    reduction and stored to each slot's output rows;
+//  * a stage wait (bulk mode) that runs out of its limit makes the warp stop issuing copies and store its
+//    remaining rows as NaN (kFaultWaitTimeout); before exiting it waits, bounded, for the copies it issued.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -33,8 +36,6 @@
 #include "launch.h"
 
 namespace q4 {
-
-static __device__ unsigned g_fault_moe;
 
 namespace {
 
@@ -58,13 +59,14 @@ struct MoEParams {
     int bulk;  // every stage is whole rows: bulk copies of quants and scales on a slot mbarrier
     uint32_t route_off, xs_off, aux_off, bar_off, slots_off;
     unsigned* fault;
+    long long wait_cycles;  // limit of one stage wait
 };
 
 // Routing tables in shared memory (route_off), each of ms = T*topk rounded up to 32 entries: slot_ids, rank,
 // owner, ucount, uoffset (ms+1), list, group_ux, group_first, group_cnt, scalars[4] (number of distinct experts,
 // number of groups), then the cumulative job cost gcum[ms+1] (64-bit), the job order of the groups gorder
-// (groups sorted by slot count) and the token of each list entry ltok.
-__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 2 * ms; }
+// (groups sorted by slot count), the token of each list entry ltok and the expert id of each group group_eid.
+__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 3 * ms; }
 
 // Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
 // (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     long long* gcum = reinterpret_cast<long long*>(route + 9 * ms + 8);  // 8-byte aligned (ms % 32 == 0)
     int* gorder = route + 9 * ms + 8 + 2 * (ms + 1) + 2;
     int* ltok = gorder + ms;  // token of each list entry (slot / topk), so stages divide nothing
+    int* group_eid = ltok + ms;  // expert id of each group
 
     // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
     // in the stream (it may have written ids, x or the outputs) before anything else.
@@ -208,10 +211,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     }
     __syncthreads();
     // group -> expert id
-    for (int gi = threadIdx.x; gi < ngroups; gi += kThreads) {
-        const int ux = group_ux[gi];
-        group_cnt[gi] |= slot_ids[list[uoffset[ux]]] << 8;  // low 8 bits: count, high bits: expert id
-    }
+    for (int gi = threadIdx.x; gi < ngroups; gi += kThreads) group_eid[gi] = slot_ids[list[uoffset[group_ux[gi]]]];
     // invalid slots: NaN outputs and a status bit (CTA 0 only)
     if (blockIdx.x == 0) {
         for (int i = 0; i < TK; ++i) {
@@ -234,9 +234,6 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const uint32_t aux = s_base + p.aux_off;
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
     const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot (bulk mode)
-    // set when a stage wait ran out: the CTA's outputs are then stored as NaN
-    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + W * D * 8);
-    if (threadIdx.x == 0) s_err = 0;
     if (p.bulk) {
         if (lane == 0) {
 #pragma unroll
@@ -262,7 +259,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         for (int c = 1; c <= kMaxC; ++c) {
             for (int c0 = 0; c0 < ngroups; c0 += 32) {
                 const int gi = c0 + lane;
-                const bool mine = gi < ngroups && (group_cnt[gi] & 0xFF) == c;
+                const bool mine = gi < ngroups && group_cnt[gi] == c;
                 const unsigned mb = __ballot_sync(0xffffffffu, mine);
                 if (mine) gorder[base + __popc(mb & ((1u << lane) - 1u))] = gi;
                 base += __popc(mb);
@@ -272,7 +269,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         long long cb = 0;
         for (int c0 = 0; c0 < ngroups; c0 += 32) {
             const int oi = c0 + lane;
-            long long v = oi < ngroups ? (long long)NP * rgs * job_cost(group_cnt[gorder[oi]] & 0xFF, PURE, p.cost_a, p.cost_b) : 0LL;
+            long long v = oi < ngroups ? (long long)NP * rgs * job_cost(group_cnt[gorder[oi]], PURE, p.cost_a, p.cost_b) : 0LL;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const long long t = __shfl_up_sync(0xffffffffu, v, off);
@@ -293,7 +290,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             if (gcum[mid] <= c) lo = mid;
             else hi = mid - 1;
         }
-        return lo * NP * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]] & 0xFF, PURE, p.cost_a, p.cost_b));
+        return lo * NP * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
     };
     const int j0 = p.deal ? gw : job_at(total_cost * gw / Wtot);
     const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : job_at(total_cost * (gw + 1) / Wtot);
@@ -331,9 +328,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     const int total = (p.deal ? (j1 - j0) : (j1 - j0)) * p.S;  // jobs of this warp x chunks
     Cursor ik = cursor_at(j0);
     int issued = 0, islot = 0;
+    bool aborted = false;  // a stage wait ran out: no more copies, the warp's remaining rows are NaN
     auto issue = [&]() {
-        if (issued < total) {
-            const int e = group_cnt[gorder[ik.grp]] >> 8;
+        if (issued < total && !aborted) {
+            const int e = group_eid[gorder[ik.grp]];
             const int r0 = ik.rg * R;
             const int rv = min(R, p.N - r0);
             const int b0 = ik.c * CB;
@@ -421,9 +419,24 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                 if (t4 == 0)
                     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
                                                                                                 : v * U + u) * 8)),
-                                 "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
+                                 "f"(block_factor(st.e)), "f"(0.0f)
                                  : "memory");
             }
+        }
+        __syncthreads();
+        // each block's -8 offset term: the unit chain on codes of 8 over its staged quads
+        for (int b = threadIdx.x; b < nb_all; b += kThreads) {
+            const int v = b / U;
+            const int u = b - v * U;
+            const int grp32 = u >> 5, ul = u & 31;
+            const uint32_t q0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8) * 32 + ul) * 16 : ((v * 8) * U + u) * 16);
+            const uint32_t qstep = XG ? 512u : (uint32_t)U * 16u;
+            float4 xq[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xq[q] = lds128f(q0 + (uint32_t)q * qstep);
+            const uint32_t a = aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul : v * U + u) * 8);
+            const float bias = q4_block_bias(xq, lds32f(a));
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 4u), "f"(bias) : "memory");
         }
     }
     __syncthreads();
@@ -440,20 +453,27 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     Cursor k = cursor_at(j0);
     int cslot = 0;
     uint32_t cphase = 0u;
+    int consumed = 0;  // stages whose wait completed (bulk mode)
     for (int g = 0; g < total; ++g) {
         issue();  // stage g + D - 1 into the slot consumed at g - 1
         // stage g has landed: its slot's mbarrier completed phase cphase (bounded wait), or its commit group
         if (p.bulk) {
-            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
+            if (!aborted) {
+                if (warp_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, p.wait_cycles)) {
+                    consumed = g + 1;
+                } else {
+                    aborted = true;
+                    if (lane == 0) atomicOr(p.fault, kFaultWaitTimeout);
+                }
+            }
         } else {
             cp_async_wait<D - 1>();
         }
         __syncwarp();
-        const bool bad = *reinterpret_cast<volatile int*>(&s_err) != 0;
+        const bool bad = aborted;
         const uint32_t slot = ring + (uint32_t)cslot * SLOT;
         const int grp = gorder[k.grp];
-        const int gc = group_cnt[grp];
-        const int cnt = gc & 0xFF;
+        const int cnt = group_cnt[grp];
         const int first = group_first[grp];
         const int r0 = k.rg * R;
         const int rv = min(R, p.N - r0);
@@ -485,7 +505,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 #pragma unroll 1
             for (int it = 0; it < UPL; ++it) {
                 const int ul = it * 32 + lane;
-                if (ul >= nb) continue;
+                if (ul >= nb || bad) continue;
                 uint4 w[RR];
                 float dsc[RR];
                 uint32_t dbits[RR];
@@ -512,14 +532,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                             const float4 xl = xq[m][it * x_it + i * qs];
                             const float4 xh = xq[m][it * x_it + (4 + i) * qs];
 #pragma unroll
-                            for (int r = 0; r < RR; ++r) {
-                                float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][m];
-                                a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
-                                a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
-                                a = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), a);
-                                a = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), a);
-                                acc[r][m] = a;
-                            }
+                            for (int r = 0; r < RR; ++r)
+                                acc[r][m] = word_fma(d8[r], xl, xh, i == 0 ? make_float2(0.f, 0.f) : acc[r][m]);
                         }
                     }
 #pragma unroll
@@ -596,51 +610,15 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             cphase ^= 1u;
         }
     }
+    // bulk copies issued but not consumed (only after a wait ran out): let them land before the CTA exits
+    if (p.bulk)
+        for (int st = consumed; st < issued; ++st)
+            if (!warp_wait_bounded(bars + 8u * (uint32_t)(st % D), (uint32_t)((st / D) & 1), kDrainCycles) &&
+                lane == 0)
+                atomicOr(p.fault, kFaultCopyLost);
 }
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
-
-// Developer override of the launch plan, read once from Q4GEMV_MOE_PLAN="variant,depth,cost_a,cost_b,deal"
-// (variant 416: 4 rows x 16 warps, otherwise 4 rows x 8 warps; the SwiGLU form: 84: 4+4 rows x 8 warps,
-// 216: 1+1 rows x 16 warps, otherwise 2+2 rows x 8 warps; depth: ignored, 2; job cost cost_a + cost_b * C; deal 1:
-// round-robin, 0: contiguous ranges). Used for tuning sweeps; the defaults come from such sweeps (12 warps,
-// 2 rows x 16 warps and depth 4 measured slower and are not compiled).
-void plan_override(int* variant, int* depth, int* cost_a, int* cost_b, int* deal) {
-    static int o_v = -1, o_d = -1, o_a = -1, o_b = -1, o_deal = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_MOE_PLAN");
-        if (e) sscanf(e, "%d,%d,%d,%d,%d", &o_v, &o_d, &o_a, &o_b, &o_deal);
-    });
-    if (o_v > 0) *variant = o_v;
-    if (o_d > 0) *depth = o_d;
-    if (o_a > 0) *cost_a = o_a;
-    if (o_b > 0) *cost_b = o_b;
-    if (o_deal >= 0) *deal = o_deal;
-}
-
-unsigned* fault_word(int device) {
-    static unsigned* ptrs[64] = {};
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[device & 63]) {
-        unsigned* p = nullptr;
-        if (cudaGetSymbolAddress((void**)&p, g_fault_moe) != cudaSuccess) return nullptr;
-        ptrs[device & 63] = p;
-    }
-    return ptrs[device & 63];
-}
-
-// Developer switch back to per-lane cp.async copies for whole-row stages, read once from Q4GEMV_MOE_BULK=0.
-bool bulk_off() {
-    static bool off = false;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_MOE_BULK");
-        off = e && e[0] == '0';
-    });
-    return off;
-}
 
 template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU, bool XG>
 cudaError_t launch_kernel_cfg(const DeviceInfo& di, const MoEParams& p, uint32_t smem, cudaStream_t s) {
@@ -663,11 +641,11 @@ cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     p.xs_off = route;
     p.aux_off = route + xsb;
     p.bar_off = route + xsb + axb;
-    p.slots_off = p.bar_off + (uint32_t)round_up(W * D * 8 + 4, 128);  // slot mbarriers and the error word
+    p.slots_off = p.bar_off + (uint32_t)round_up(W * D * 8, 128);  // slot mbarriers
     const uint32_t smem = p.slots_off + (uint32_t)(W * D) * moe_slot_bytes(SWIGLU ? 2 * R : R, UPL);
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     p.S = (p.nblk + 32 * UPL - 1) / (32 * UPL);
-    p.bulk = (p.dcopy && p.S == 1 && p.nblk == 32 * UPL && !bulk_off()) ? 1 : 0;
+    p.bulk = (p.dcopy && p.S == 1 && p.nblk == 32 * UPL) ? 1 : 0;
     // grouped staging whenever the blocks fill whole groups of 32 (no padding); the pure read stages nothing
     if constexpr (!PURE) {
         if (p.nblk % 32 == 0) return launch_kernel_cfg<R, W, D, UPL, PURE, SWIGLU, true>(di, p, smem, s);
@@ -722,39 +700,28 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.ms = (T * topk + 31) / 32 * 32;
     p.dcopy = (p.nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(d_gate) & 15u) == 0) &&
               ((reinterpret_cast<uintptr_t>(d_up) & 15u) == 0);
-    p.fault = fault_word(di.device);
+    p.fault = device_fault_word(di.device);
+    p.wait_cycles = wait_limit_cycles();
     if (!p.fault) return cudaErrorInvalidSymbol;
-    // defaults from sweeps over routing seeds: 16 warps x 4 rows, ring depth 2, contiguous cost-balanced job
+    // plans from sweeps over routing seeds: 16 warps x 4 rows, ring depth 2, contiguous cost-balanced job
     // ranges; the SwiGLU form (4 gate + 4 up rows per slot) 8 warps with round-robin dealing
-    int variant = swiglu ? 84 : 416, depth = 2;
+    const int depth = 2;
     p.cost_a = 9;
     p.cost_b = 5;
     p.deal = swiglu ? 1 : 0;
-    plan_override(&variant, &depth, &p.cost_a, &p.cost_b, &p.deal);
     // 16 warps x 4 rows when it fits beside the staged tokens, else 8 warps x 4 rows (the same for the pure
     // read, which streams like the GEMV plan)
-    e = cudaErrorNotSupported;
     if (pure_read) {
-        if (variant == 416) e = launch<4, 16, true>(di, p, depth, s);
-        if (e == cudaErrorNotSupported) e = launch<4, 8, true>(di, p, depth, s);
-        return e;
+        e = launch<4, 16, true>(di, p, depth, s);
+        return e == cudaErrorNotSupported ? launch<4, 8, true>(di, p, depth, s) : e;
     }
     if (swiglu) {  // R gate + R up rows per slot
-        if (variant == 216) return launch<1, 16, false, true>(di, p, depth, s);
-        if (variant == 84) e = launch<4, 8, false, true>(di, p, depth, s);
-        if (e == cudaErrorNotSupported) e = launch<2, 8, false, true>(di, p, depth, s);
-        return e;
+        e = launch<4, 8, false, true>(di, p, depth, s);
+        return e == cudaErrorNotSupported ? launch<2, 8, false, true>(di, p, depth, s) : e;
     }
-    if (variant == 416) e = launch<4, 16, false>(di, p, depth, s);
-    if (e == cudaErrorNotSupported) e = launch<4, 8, false>(di, p, depth, s);
-    return e;
+    e = launch<4, 16, false>(di, p, depth, s);
+    return e == cudaErrorNotSupported ? launch<4, 8, false>(di, p, depth, s) : e;
 }
 
-cudaError_t read_and_clear_fault_moe(unsigned* out) {
-    unsigned zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_moe, sizeof(unsigned));
-    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fault_moe, &zero, sizeof(unsigned));
-    return e;
-}
 
 }  // namespace q4

@@ -1,19 +1,36 @@
 // Planar Q4 decode GEMV for sm_103a: the single-vector launch plans, the dispatch over batch widths, the
-// pure-read ceiling instrument and the bit-exact dequant dump. The kernel itself is in q4_dense.cuh.
+// pure-read ceiling instrument and the bit-exact dequant dump. The kernels are in q4_xr.cuh (one vector, input
+// in registers) and q4_dense.cuh (the general and batched kernel).
 #include <cstdio>
 #include <cstdlib>
 
 #include "q4_dense.cuh"
+#include "q4_xr.cuh"
 
 namespace q4 {
 namespace dense {
 
-// One vector: 16 warps x 2 rows per lane, whole rows per stage up to K = 4096 (4 units per lane; longer rows in
-// 128-block chunks), ring depth 2 (3 on request through Q4GEMV_Q4_DEPTH). Measured slower at 14336x4096:
-// 16 warps x 1 row, 24 warps x 1 row, 10-14 warps x 2 rows, 8 warps x 4 rows with the input in registers,
-// two accumulation chains per row, rings of depth 3 to 8.
+// The register-input plan for one vector: 8 warps x 4 rows per job, ring depth 2 (one stage requested before the
+// dependency wait), for K/32 a multiple of 8 up to 128 blocks with 16-byte aligned scales. Measured on the
+// 14336x4096 workload against 3 rows at depth 3, 5 rows, 2 rows at depth 4, 6 to 12 warps and the shared-memory
+// input plan (16 warps x 2 rows); requesting the whole ring before the wait was slower (the copies delay the
+// input's staging and the release of the dependent launch).
+template <bool PURE>
+cudaError_t launch_xr_plan(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X,
+                           int N, int K, cudaStream_t s) {
+    const int nblk = K / 32;
+    if (nblk > 96) return xr::launch_xr<4, 8, 2, 4, 1, PURE>(di, Y, qs, d, X, N, K, s);
+    if (nblk > 64) return xr::launch_xr<4, 8, 2, 3, 1, PURE>(di, Y, qs, d, X, N, K, s);
+    if (nblk > 32) return xr::launch_xr<4, 8, 2, 2, 1, PURE>(di, Y, qs, d, X, N, K, s);
+    return xr::launch_xr<4, 8, 2, 1, 1, PURE>(di, Y, qs, d, X, N, K, s);
+}
+
+// One vector: the register-input plan where it applies, else 16 warps x 2 rows per lane, whole rows per stage
+// up to K = 4096 (longer rows in 128-block chunks), ring depth 2.
 cudaError_t gemv_v1(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int N,
                     int K, cudaStream_t s) {
+    cudaError_t e = launch_xr_plan<false>(di, Y, qs, d, X, N, K, s);
+    if (e != cudaErrorNotSupported) return e;
     return launch<1, 2, 16, 3, false>(di, Y, qs, d, X, N, K, 2, 4, s);
 }
 
@@ -31,12 +48,14 @@ cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const
     return cudaErrorInvalidValue;
 }
 
-// The same streaming as the single-vector plan (16 warps x 2 rows, whole rows per stage, ring depth 2), no
-// math.
+// The same streaming as the single-vector plan (the register-input plan where it applies, else 16 warps x 2
+// rows, whole rows per stage, ring depth 2), no math.
 cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s) {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess) return e;
+    e = dense::launch_xr_plan<true>(di, sink, qs, d, nullptr, N, K, s);
+    if (e != cudaErrorNotSupported) return e;
     return dense::launch<1, 2, 16, 3, true>(di, sink, qs, d, nullptr, N, K, 2, 4, s);
 }
 

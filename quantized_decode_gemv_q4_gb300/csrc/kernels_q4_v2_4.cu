@@ -8,24 +8,9 @@ namespace dense {
 cudaError_t gemv_v2_4(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
                       int N, int K, cudaStream_t s) {
     switch (V) {
-        case 2:
-            switch (batched_variant()) {
-                case 216: return launch<2, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<2, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<2, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
-        case 3:
-            switch (batched_variant()) {
-                case 216: return launch<3, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<3, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<3, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
-        case 4:
-            switch (batched_variant()) {
-                case 216: return launch<4, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<4, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<4, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
+        case 2: return launch<2, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
+        case 3: return launch<3, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
+        case 4: return launch<4, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -9,30 +9,10 @@ namespace dense {
 cudaError_t gemv_v5_8(const DeviceInfo& di, float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V,
                       int N, int K, cudaStream_t s) {
     switch (V) {
-        case 5:
-            switch (batched_variant()) {
-                case 216: return launch<5, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<5, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<5, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
-        case 6:
-            switch (batched_variant()) {
-                case 216: return launch<6, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<6, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<6, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
-        case 7:
-            switch (batched_variant()) {
-                case 216: return launch<7, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<7, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<7, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
-        case 8:
-            switch (batched_variant()) {
-                case 216: return launch<8, 2, 16, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                case 28: return launch<8, 2, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-                default: return launch<8, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
-            }
+        case 5: return launch<5, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
+        case 6: return launch<6, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
+        case 7: return launch<7, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
+        case 8: return launch<8, 4, 8, 2, false>(di, Y, qs, d, X, N, K, 2, 4, s);
         default: return cudaErrorInvalidValue;
     }
 }

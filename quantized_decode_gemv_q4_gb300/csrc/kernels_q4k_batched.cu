@@ -7,14 +7,16 @@
 //
 // Kernel shape (one persistent CTA of W warps per SM), the Q4_K kernel's with V vectors:
 //  * the V vectors are staged once per CTA, each 32-element sub-block with its own exponent bound e_{j,v}
-//    (bias-free decode, device_common.cuh), beside (S_{j,v}, 2^(22+e_{j,v}));
+//    (bias-free decode, device_common.cuh); beside each unit (16 quant bytes: half of sub-block 2c in the low
+//    nibbles, the same half of 2c+1 in the high ones) sit (S_lo, S_hi, f_lo, f_hi): f = 2^(22+e) of the two
+//    sub-blocks and S = f times the unit's FMA chain run on codes of 1 over each half;
 //  * each warp streams R rows (whole rows when they fit) through its own ring of cp.async slots;
 //  * lane l takes unit l (+32, ...) of every row: chunk c = (l%8)/2, half l%2; the 8 lanes of a super-block
 //    each decode one sub-block's header entry (d*sc_j and dmin*m_j), shared with the group by shuffles;
 //  * per word: one shift + eight ANDs per row, then for each vector two staged-input loads (shared by the R
-//    rows) and four packed FMAs per row into one accumulator per sub-block; per unit and vector the two
-//    accumulators fold with d*sc*2^(22+e) of their sub-block, and each lane adds dmin*m_j*S_{j,v} of its own
-//    sub-block (the warp reduction sums the eight);
+//    rows) and four packed FMAs per row into one accumulator per sub-block half; per unit and vector the two
+//    halves fold as fl(d*sc*f * A) - fl(dmin*m * S) with unfused rounded operations, so halves whose weights are all zero
+//    (sc = m = 0, or a constant power-of-two code with d*sc*q = dmin*m) contribute exactly zero;
 //  * the R*V totals are summed over the warp with the transposing shuffle reduction and stored.
 #include <algorithm>
 #include <mutex>
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
 
     const uint32_t s_base = smem_addr(smem);
     const uint32_t xs = s_base + p.xs_off;      // float[V][8 quads][U][4]
-    const uint32_t ssum = s_base + p.ssum_off;  // float2[V][K/32]: (S_j, 2^(22+e_j))
+    const uint32_t ssum = s_base + p.ssum_off;  // float4[V][K/32] per unit: (S_lo, S_hi, f_lo, f_hi)
     const uint32_t ring = s_base + p.slots_off + (uint32_t)(warp * D * p.slot_bytes);
 
     const int gw = warp * (int)gridDim.x + (int)blockIdx.x;
@@ -109,23 +111,41 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + U * 16u), "f"(st.b.x), "f"(st.b.y),
                          "f"(st.b.z), "f"(st.b.w)
                          : "memory");
-            if (t4 == 0)
-                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ssum + (uint32_t)jsv * 8u), "f"(st.sum),
-                             "f"(block_factor(st.e))
-                             : "memory");
+            if (t4 == 0) {
+                // f of sub-block js goes to both units of its chunk (.z for the low sub-block, .w for the high)
+                const uint32_t ua = ssum + ((uint32_t)v * U + (uint32_t)(js & ~1)) * 16u + 8u + (uint32_t)k * 4u;
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(ua), "f"(block_factor(st.e)) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(ua + 16u), "f"(block_factor(st.e)) : "memory");
+            }
+        }
+        __syncthreads();
+        // S of each unit's two halves: the unit chain on codes of 1 (low pairs over quads 0..3, high over 4..7)
+        const Word8s c1 = decode_word_sub(0x11111111u);
+        for (int t = threadIdx.x; t < V * (int)U; t += kThreads) {
+            const uint32_t v = (uint32_t)t / U, u = (uint32_t)t - v * U;
+            float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 xl = lds128f(xs + xs_index(v, (uint32_t)i, u, U) * 4u);
+                const float4 xh = lds128f(xs + xs_index(v, (uint32_t)(4 + i), u, U) * 4u);
+                a = ffma2(c1.lo01, make_float2(xl.x, xl.y), a);
+                a = ffma2(c1.lo23, make_float2(xl.z, xl.w), a);
+                b = ffma2(c1.hi01, make_float2(xh.x, xh.y), b);
+                b = ffma2(c1.hi23, make_float2(xh.z, xh.w), b);
+            }
+            const uint32_t ua = ssum + ((uint32_t)v * U + u) * 16u;
+            const float2 f = lds64f(ua + 8u);
+            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ua), "f"((a.x + a.y) * f.x), "f"((b.x + b.y) * f.y)
+                         : "memory");
         }
     }
     __syncthreads();
 
     float2 tot[R][V];
-    float mins[R][V];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-            tot[r][v] = make_float2(0.f, 0.f);
-            mins[r][v] = 0.f;
-        }
+        for (int v = 0; v < V; ++v) tot[r][v] = make_float2(0.f, 0.f);
 
     const uint32_t cpos = (uint32_t)(lane & 7);
     const uint32_t jj = cpos & 3u;
@@ -155,7 +175,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             const int sbl = valid ? (ul >> 3) : 0;
             const uint32_t u = (uint32_t)(8 * (sb0 + sbl)) + cpos;  // unit index = sub-block index of j = cpos
             uint4 w[R];
-            float dlo[R], dhi[R], dmm[R];
+            float dlo[R], dhi[R], mlo[R], mhi[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t it = (uint32_t)(r * cs + sbl);
@@ -165,9 +185,11 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
                 const uint32_t mw = cpos < 4 ? (hdr.z & 0x3F3F3F3Fu)
                                              : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
                 const float dsc = f16_bits_to_f32(hdr.x) * byte_as_float_b(scw, (int)jj);
-                dmm[r] = f16_bits_to_f32(hdr.x >> 16) * byte_as_float_b(mw, (int)jj);
+                const float dmm = -(f16_bits_to_f32(hdr.x >> 16) * byte_as_float_b(mw, (int)jj));
                 dlo[r] = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos & ~1u));
                 dhi[r] = __shfl_sync(0xffffffffu, dsc, gbase + (int)(cpos | 1u));
+                mlo[r] = __shfl_sync(0xffffffffu, dmm, gbase + (int)(cpos & ~1u));
+                mhi[r] = __shfl_sync(0xffffffffu, dmm, gbase + (int)(cpos | 1u));
                 w[r] = lds128(slot + it * 144u + 16u + cpos * 16u);
             }
             float2 aL[R][V], aH[R][V];
@@ -198,16 +220,16 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             if (valid) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    // (S, f) of sub-blocks 2c and 2c+1 of this super-block for vector v
-                    const float4 sf = lds128f(ssum + ((uint32_t)v * (uint32_t)nsub + (u & ~1u)) * 8u);
-                    const float s_own = (cpos & 1u) ? sf.z : sf.x;
+                    // (S_lo, S_hi, f_lo, f_hi) of this unit for vector v
+                    const float4 sf = lds128f(ssum + ((uint32_t)v * U + u) * 16u);
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float fl = dlo[r] * sf.y;
-                        const float fh = dhi[r] * sf.w;
-                        tot[r][v] = ffma2(make_float2(fl, fl), aL[r][v], tot[r][v]);
-                        tot[r][v] = ffma2(make_float2(fh, fh), aH[r][v], tot[r][v]);
-                        mins[r][v] = fmaf(dmm[r], s_own, mins[r][v]);
+                        // fl(d*sc*f * A) - fl(dmin*m * S) per half (d*sc*f and dmin*m are exact), with scalar
+                        // rounded operations that the compiler never fuses into an FMA
+                        const float ul = __fmul_rn(dlo[r] * sf.z, aL[r][v].x + aL[r][v].y);
+                        const float uh = __fmul_rn(dhi[r] * sf.w, aH[r][v].x + aH[r][v].y);
+                        tot[r][v].x = __fadd_rn(tot[r][v].x, __fadd_rn(ul, __fmul_rn(mlo[r], sf.x)));
+                        tot[r][v].y = __fadd_rn(tot[r][v].y, __fadd_rn(uh, __fmul_rn(mhi[r], sf.y)));
                     }
                 }
             }
@@ -225,9 +247,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    vals[r * V + v] = (tot[r][v].x + tot[r][v].y) - mins[r][v];
+                    vals[r * V + v] = tot[r][v].x + tot[r][v].y;
                     tot[r][v] = make_float2(0.f, 0.f);
-                    mins[r][v] = 0.f;
                 }
             warp_transpose_reduce<P2>(vals, lane);
             const int idx = lane >> (5 - L2);
@@ -248,7 +269,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
 
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-// Shared memory: [staged X V*K*4][(S, factor) V*K/32*8][W rings of D slots of R rows x CS super-blocks];
+// Shared memory: [staged X V*K*4][(S_lo, S_hi, f_lo, f_hi) per unit V*K/32*16][W rings of D slots of R rows x CS super-blocks];
 // whole rows first, then smaller chunks, then depth 2.
 template <int V, int R, int W>
 cudaError_t run_batched(const DeviceInfo& di, float* Y, const uint8_t* w, const float* X, int N, int K,
@@ -262,7 +283,7 @@ cudaError_t run_batched(const DeviceInfo& di, float* Y, const uint8_t* w, const 
     p.K = K;
     p.nsb = nsb;
     const uint32_t xsb = (uint32_t)round_up(V * K * 4, 128);
-    const uint32_t ssb = (uint32_t)round_up(V * (K / 32) * 8, 128);
+    const uint32_t ssb = (uint32_t)round_up(V * (K / 32) * 16, 128);
     p.xs_off = 0;
     p.ssum_off = xsb;
     p.slots_off = xsb + ssb;

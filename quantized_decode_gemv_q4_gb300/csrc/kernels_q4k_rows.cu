@@ -12,13 +12,19 @@
 //    coalesced 16-byte cp.async (nine per lane) into its own ring of D slots;
 //  * prologue: the first stages are issued, then (after the previous kernel in the stream is done) sum(x^2),
 //    r = rsqrt(sum/K + eps), xhat = x * r * gamma staged per 32-element sub-block j, pre-scaled for the
-//    bias-free decode with its own exponent bound e_j, next to (S_j = sum of xhat over j, 2^(22+e_j));
+//    bias-free decode with its own exponent bound e_j, next to (S_j, 2^(22+e_j)) where S_j * 2^(-22-e_j) is the
+//    sub-block's FMA chain run on codes of 1 (so it matches a sub-block of equal unit codes bit for bit);
 //  * lane l decodes the header of its own row's super-block once (eight 6-bit scales and mins), then runs
 //    over the four chunks: one shift and eight ANDs per word, packed fp32x2 FMAs against the staged input
 //    (every lane reads the same input quads, so each shared load is one broadcast wavefront), one
-//    accumulator per sub-block folded with d*sc_j*2^(22+e_j); the min terms are folded once per super-block;
+//    accumulator A_j per sub-block; each sub-block is folded as fl(d*sc_j*2^(22+e_j) * A_j) -
+//    fl(dmin*m_j * S_j) with unfused rounded operations, so a sub-block whose weights d*sc_j*q - dmin*m_j are all zero
+//    (sc_j = m_j = 0, or a constant power-of-two code with d*sc_j*q = dmin*m_j) contributes exactly zero;
 //  * per tile the warps' per-lane partial sums meet in shared memory (double-buffered by tile parity, one
 //    CTA barrier per tile) and one warp, rotating with the tile, adds them in warp order and stores the rows.
+//  * a stage wait that runs out of its limit makes the warp stop issuing copies and contribute NaN partials, so
+//    every row the CTA stores from then on is NaN (kFaultWaitTimeout); before exiting the warp waits, bounded,
+//    for the copies it had issued.
 // Inputs whose staged value reaches 2^83 in magnitude are outside the supported range (non-finite result).
 #include <algorithm>
 #include <cstdio>
@@ -53,6 +59,8 @@ struct RowParams {
     int N, K, nsb;
     int tiles;           // ceil(N / rows per tile)
     int nb;              // tiles per reduction group, 1..kGroupMax
+    long long wait_cycles;  // limit of one stage wait
+    unsigned* fault;        // device fault word
     uint32_t xs_off, ss_off, red_off, bar_off, slots_off;
 };
 
@@ -90,7 +98,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
     const uint64_t pol = policy_evict_first();
     const uint32_t bars = smem_addr(smem) + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot
     // set when a stage wait ran out: the CTA's rows are then stored as NaN
-    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + kMaxWarps * 3 * 8);
+    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + kMaxWarps * 3 * 8);  // some warp's wait ran out
     if (threadIdx.x == 0) s_err = 0;
     if constexpr (TMA) {
         if (lane == 0) {
@@ -123,8 +131,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
     const int total = my_tiles * spb;
 
     int itile = (int)blockIdx.x, ik = 0, islot = 0, iss = 0;
+    bool aborted = false;  // a stage wait ran out: no more copies, this warp's partials are NaN
     auto issue = [&]() {
-        if (iss < total) {
+        if (iss < total && !aborted) {
             const int r0 = itile * TR;
             const int nv = p.N - r0;
             const int sb = warp + ik * nw;
@@ -219,20 +228,43 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
             const Stage4 st = stage_block4(xa, xb, js & 1);
             xs[js * 8 + 2 * t4] = st.a;
             xs[js * 8 + 2 * t4 + 1] = st.b;
-            if (t4 == 0) ssum[js] = make_float2(st.sum, block_factor(st.e));
+            if (t4 == 0) ssum[js] = make_float2(0.f, block_factor(st.e));
+        }
+        __syncthreads();
+        // S_j: the sub-block's chain (quads 0..7, each as its low or high pair) on codes of 1, times 2^(22+e_j)
+        const Word8s c1 = decode_word_sub(0x11111111u);
+        for (int js = threadIdx.x; js < nsub; js += nthreads) {
+            const float2 p01 = (js & 1) ? c1.hi01 : c1.lo01, p23 = (js & 1) ? c1.hi23 : c1.lo23;
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = xs[js * 8 + q];
+                a = ffma2(p01, make_float2(v.x, v.y), a);
+                a = ffma2(p23, make_float2(v.z, v.w), a);
+            }
+            ssum[js].x = (a.x + a.y) * ssum[js].y;
         }
     }
     __syncthreads();
 
-    float tot = 0.f;
+    float2 tot2 = make_float2(0.f, 0.f);
     uint32_t fold = 0u;
     int tile = (int)blockIdx.x, k = 0, cslot = 0, tcount = 0;
     uint32_t cphase = 0u;
+    int consumed = 0;  // stages whose wait completed (tensor-copy mode)
     for (int g = 0; g < total; ++g) {
         issue();  // stage g + D - 1 into the slot consumed at g - 1
         if constexpr (TMA) {
             // stage g has landed once its slot's mbarrier completes phase cphase; the wait is bounded
-            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
+            if (!aborted) {
+                if (warp_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, p.wait_cycles)) {
+                    consumed = g + 1;
+                } else {
+                    aborted = true;
+                    s_err = 1;
+                    if (lane == 0) atomicOr(p.fault, kFaultWaitTimeout);
+                }
+            }
         } else {
             cp_async_wait<D - 1>();  // stage g has landed
         }
@@ -240,7 +272,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
         const uint8_t* const sp = ring_p + (size_t)cslot * kSlot + (size_t)lane * kSB;
         const int sb = warp + k * nw;
         const uint4 hdr = *reinterpret_cast<const uint4*>(sp);
-        if constexpr (PURE) {
+        if (aborted) {
+            // no compute after a timed-out wait; the tile's rows are stored as NaN
+        } else if constexpr (PURE) {
             uint32_t f = hdr.x ^ hdr.y ^ hdr.z ^ hdr.w;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -258,16 +292,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
             const uint32_t m47 = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
             const float4* const xq = reinterpret_cast<const float4*>(smem + p.xs_off) + sb * 64;
             const float4* const sq = reinterpret_cast<const float4*>(smem + p.ss_off) + sb * 4;
-            float msum = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float4 sf = sq[c];  // (S, 2^(22+e)) of sub-blocks 2c and 2c+1
                 const uint32_t scw = c < 2 ? sc03 : sc47;
                 const uint32_t mw = c < 2 ? m03 : m47;
-                const float dlo = (d * sbyte(scw, (2 * c) & 3)) * sf.y;
-                const float dhi = (d * sbyte(scw, (2 * c + 1) & 3)) * sf.w;
-                msum = fmaf(sbyte(mw, (2 * c) & 3), sf.x, msum);
-                msum = fmaf(sbyte(mw, (2 * c + 1) & 3), sf.z, msum);
+                // d*sc_j*2^(22+e_j) and -dmin*m_j, both exact (products of at most 17 significant bits)
+                const float2 dsc = make_float2((d * sbyte(scw, (2 * c) & 3)) * sf.y, (d * sbyte(scw, (2 * c + 1) & 3)) * sf.w);
+                const float2 mn = make_float2(-dmin * sbyte(mw, (2 * c) & 3), -dmin * sbyte(mw, (2 * c + 1) & 3));
                 float2 aL = make_float2(0.f, 0.f), aH = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -283,10 +315,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
                         aH = ffma2(d8.hi23, make_float2(xh.z, xh.w), aH);
                     }
                 }
-                tot = fmaf(dlo, aL.x + aL.y, tot);
-                tot = fmaf(dhi, aH.x + aH.y, tot);
+                // fl(dsc * A) - fl(dmin * m * S) per sub-block, then into the running pair; scalar rounded
+                // operations, which the compiler never fuses into an FMA (a fused form would leave the
+                // product's rounding error instead of an exact zero)
+                tot2.x = __fadd_rn(tot2.x, __fadd_rn(__fmul_rn(dsc.x, aL.x + aL.y), __fmul_rn(mn.x, sf.x)));
+                tot2.y = __fadd_rn(tot2.y, __fadd_rn(__fmul_rn(dsc.y, aH.x + aH.y), __fmul_rn(mn.y, sf.z)));
             }
-            tot = fmaf(-dmin, msum, tot);
         }
         __syncwarp();  // every lane is done with this slot before a later stage reuses it
 
@@ -296,8 +330,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
             // rotating with the tile, adds the partials in warp order and stores the tile's rows
             const int gi = tcount % p.nb;
             float* const gbuf = red + ((tcount / p.nb) & 1) * (kGroupMax * kMaxWarps * 32);
-            gbuf[(gi * kMaxWarps + warp) * 32 + lane] = PURE ? __uint_as_float(fold) : tot;
-            tot = 0.f;
+            gbuf[(gi * kMaxWarps + warp) * 32 + lane] = aborted ? NAN : PURE ? __uint_as_float(fold) : tot2.x + tot2.y;
+            tot2 = make_float2(0.f, 0.f);
             fold = 0u;
             if (gi == p.nb - 1 || tcount == my_tiles - 1) {
                 __syncthreads();
@@ -334,6 +368,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
             cphase ^= 1u;
         }
     }
+    // tensor copies issued but not consumed (only after a wait ran out): let them land before the CTA exits
+    if constexpr (TMA)
+        for (int st = consumed; st < iss; ++st)
+            if (!warp_wait_bounded(bars + 8u * (uint32_t)(st % D), (uint32_t)((st / D) & 1), kDrainCycles) &&
+                lane == 0)
+                atomicOr(p.fault, kFaultCopyLost);
 }
 
 inline uint32_t round_up_u32(uint32_t a, uint32_t b) { return (a + b - 1) / b * b; }
@@ -349,22 +389,6 @@ cudaError_t launch_rows_fixed(const DeviceInfo& di, const RowParams& p, int nw, 
     if (err != cudaSuccess) return err;
     const int grid = std::min(di.sm_count, p.tiles);
     return launch_kernel(kern, grid, nw * 32, smem, s, p);
-}
-
-// Developer override of the ring depth, warp count, reduction group and copy engine (1: bulk tensor copies,
-// 0: per-lane cp.async), read once from Q4GEMV_Q4K_ROWS="depth,warps,group,tma". Used for tuning sweeps;
-// the defaults come from such sweeps.
-void rows_override(int* depth, int* warps, int* group, int* tma) {
-    static int o_d = -1, o_w = -1, o_g = -1, o_t = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_Q4K_ROWS");
-        if (e) sscanf(e, "%d,%d,%d,%d", &o_d, &o_w, &o_g, &o_t);
-    });
-    if (o_d > 0) *depth = o_d;
-    if (o_w > 0) *warps = o_w;
-    if (o_g > 0) *group = o_g;
-    if (o_t >= 0) *tma = o_t;
 }
 
 // Tensor map of a Q4_K weight matrix as a 2-D byte tensor [N][K/256*144], box 144 bytes x `rows`, rows past
@@ -450,30 +474,23 @@ cudaError_t run_rows(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1,
     p.K = K;
     p.nsb = K / 256;
     p.tiles = (N + 32 / NS - 1) / (32 / NS);
-    int depth = 2, want_w = kMaxWarps, nb = kGroupMax, tma = 1;
-    rows_override(&depth, &want_w, &nb, &tma);
-    p.nb = std::max(1, std::min(kGroupMax, nb));
-    if (tma) {
-        if (!weight_map(&p.tm0, w0, N, K, 32 / NS)) return cudaErrorNotSupported;
-        if (NS == 2 && !weight_map(&p.tm1, w1, N, K, 32 / NS)) return cudaErrorNotSupported;
-    }
-    const int per_warp = (p.nsb + std::min(want_w, kMaxWarps) - 1) / std::min(want_w, kMaxWarps);
+    p.wait_cycles = wait_limit_cycles();
+    p.nb = kGroupMax;
+    p.fault = device_fault_word(di.device);
+    if (!p.fault) return cudaErrorInvalidSymbol;
+    if (!weight_map(&p.tm0, w0, N, K, 32 / NS)) return cudaErrorNotSupported;
+    if (NS == 2 && !weight_map(&p.tm1, w1, N, K, 32 / NS)) return cudaErrorNotSupported;
+    const int per_warp = (p.nsb + kMaxWarps - 1) / kMaxWarps;
     const int nw = (p.nsb + per_warp - 1) / per_warp;
     p.xs_off = 0;
     p.ss_off = PURE ? 0u : (uint32_t)K * 4u;
     p.red_off = p.ss_off + (PURE ? 0u : round_up_u32((uint32_t)(K / 32) * 8u, 128u));
     p.bar_off = p.red_off + round_up_u32((uint32_t)(2 * kGroupMax * kMaxWarps * 32 + kMaxWarps) * 4u, 128u);
     p.slots_off = p.bar_off + round_up_u32((uint32_t)(kMaxWarps * 3 * 8 + 4), 128u);
+    // ring depth 2 (the measured best), fewer warps for the longest inputs
     for (int w = nw; w >= 1; --w) {
-        for (int dd = std::min(3, std::max(2, depth)); dd >= 2; --dd) {
-            const uint32_t smem = p.slots_off + (uint32_t)(w * dd) * kSlot;
-            if (smem > (uint32_t)di.max_smem_optin) continue;
-            if (dd == 3)
-                return tma ? launch_rows_fixed<NS, 3, PURE, true>(di, p, w, smem, s)
-                           : launch_rows_fixed<NS, 3, PURE, false>(di, p, w, smem, s);
-            return tma ? launch_rows_fixed<NS, 2, PURE, true>(di, p, w, smem, s)
-                       : launch_rows_fixed<NS, 2, PURE, false>(di, p, w, smem, s);
-        }
+        const uint32_t smem = p.slots_off + (uint32_t)(w * 2) * kSlot;
+        if (smem <= (uint32_t)di.max_smem_optin) return launch_rows_fixed<NS, 2, PURE, true>(di, p, w, smem, s);
     }
     return cudaErrorNotSupported;
 }

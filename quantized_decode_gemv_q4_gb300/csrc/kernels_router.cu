@@ -14,7 +14,9 @@
 //    the warp sums the lanes; the logits go to the CTA's own shared memory;
 //  * after a cluster barrier, CTA 0 gathers the other CTAs' logits through distributed shared memory; a second
 //    barrier releases them; its warp 0 then takes the softmax over all E logits (max subtracted) and K arg-max
-//    passes (ties to the lower index), and writes ids and weights (the logits, when asked, come from every CTA).
+//    passes over a 64-bit key (the logit's order-preserving bits, a NaN below every other value, then the
+//    complement of the index, so ties go to the lower index); taken experts are marked in per-lane bit masks,
+//    and it writes ids and weights (the logits, when asked, come from every CTA).
 #include <algorithm>
 #include <mutex>
 
@@ -92,9 +94,19 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
                              : "memory");
                 if (t4 == 0)
                     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset(0u, (uint32_t)blk, 1u)),
-                                 "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
+                                 "f"(block_factor(st.e)), "f"(0.0f)
                                  : "memory");
             }
+        }
+        __syncthreads();
+        // each block's -8 offset term: the unit chain on codes of 8 over its staged quads
+        for (int b = threadIdx.x; b < p.nblk; b += W * 32) {
+            float4 xq[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xq[q] = lds128f(xs + xs_chunk_offset(0u, (uint32_t)q, (uint32_t)b, 1u));
+            const uint32_t a = aux + aux_offset(0u, (uint32_t)b, 1u);
+            const float bias = q4_block_bias(xq, lds32f(a));
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 4u), "f"(bias) : "memory");
         }
     }
     __syncthreads();
@@ -131,10 +143,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
                     const Word8s d8 = decode_word_sub(i == 0 ? w[j].x : i == 1 ? w[j].y : i == 2 ? w[j].z : w[j].w);
                     const float4 xl = lds128f(xa + (uint32_t)i * 512u);
                     const float4 xh = lds128f(xa + (uint32_t)(4 + i) * 512u);
-                    acc = ffma2(d8.lo01, make_float2(xl.x, xl.y), acc);
-                    acc = ffma2(d8.lo23, make_float2(xl.z, xl.w), acc);
-                    acc = ffma2(d8.hi01, make_float2(xh.x, xh.y), acc);
-                    acc = ffma2(d8.hi23, make_float2(xh.z, xh.w), acc);
+                    acc = word_fma(d8, xl, xh, acc);
                 }
                 const float2 fa = lds64f(aux + aux_offset(0u, (uint32_t)u, 1u));
                 const float v = f16_bits_to_f32(db[j]) * fmaf(acc.x + acc.y, fa.x, fa.y);
@@ -149,10 +158,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
         }
         if (lane == 0) {
             if (p.logits) p.logits[(size_t)t * p.E + ea] = ta;
-            lg[ea] = ta != ta ? -INFINITY : ta;  // a NaN logit ranks last
+            lg[ea] = ta;
             if (hb) {
                 if (p.logits) p.logits[(size_t)t * p.E + eb] = tb;
-                lg[eb] = tb != tb ? -INFINITY : tb;
+                lg[eb] = tb;
             }
         }
     }
@@ -177,38 +186,36 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
         for (int e = lane; e < p.E; e += 32) z += expf(lg[e] - mx);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-        // K arg-max passes over the untaken experts (a taken expert's logit becomes NaN, which never compares
-        // greater or equal); ties go to the lower index. At most K-1 <= E-1 are taken, so a pass always finds one.
+        // K arg-max passes over the untaken experts: lane l holds experts l + 32 j, taken ones marked in
+        // tk[j / 32] bit j % 32 (E <= 4096); topk <= E, so a pass always finds an untaken expert
+        uint32_t tk[4] = {0u, 0u, 0u, 0u};
         float wsum = 0.f;
         float wsel = 0.f;
         int isel = 0;
         for (int i = 0; i < p.topk; ++i) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int e = lane; e < p.E; e += 32) {
+            unsigned long long best = 0ull;
+            for (int e = lane, j = 0; e < p.E; e += 32, ++j) {
+                if ((tk[j >> 5] >> (j & 31)) & 1u) continue;
                 const float v = lg[e];
-                if (v > bv || (v == bv && e < bi)) {
-                    bv = v;
-                    bi = e;
-                }
+                const uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);  // -0 ranks with +0
+                const uint32_t key = v != v ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+                const unsigned long long c = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+                best = c > best ? c : best;
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+                best = o > best ? o : best;
             }
-            const float pw = expf(bv - mx) / z;
+            const int bi = best != 0ull ? (int)(0xFFFFFFFFu - (uint32_t)best) : -1;
+            const bool found = bi >= 0 && bi < p.E;
+            const float pw = found ? expf(lg[bi] - mx) / z : NAN;
             wsum += pw;
             if (lane == i % 32) {  // lane j holds pick j of the current group of 32 picks
                 wsel = pw;
-                isel = bi;
+                isel = found ? bi : -1;
             }
-            if (lane == 0) lg[bi] = __int_as_float(0x7fc00000);
-            __syncwarp();
+            if (found && lane == (bi & 31)) tk[(bi >> 5) >> 5] |= 1u << ((bi >> 5) & 31);
             if (i % 32 == 31 || i == p.topk - 1) {
                 const int base = i - (i % 32);
                 if (lane <= i % 32) {

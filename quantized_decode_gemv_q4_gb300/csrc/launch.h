@@ -20,6 +20,13 @@ cudaError_t current_device_info(DeviceInfo* out);
 // Process-wide launch-overlap setting (programmatic dependent launch), set through the C ABI.
 bool launch_overlap();
 
+// Process-wide limit, in SM cycles, of one kernel wait for a weight stage (q4_set_wait_limit); default 4e9.
+long long wait_limit_cycles();
+
+// Device address of the fault word of `device` (the current device), which kernels OR kFault* bits into; nullptr
+// when it cannot be resolved. The word is read and cleared by q4_device_faults.
+unsigned* device_fault_word(int device);
+
 // Launch a GEMV kernel; with launch overlap on, it may start while the previous kernel in the stream is
 // still running (the kernel waits for it before touching inputs or outputs, see grid_dependency_wait).
 template <typename Kernel, typename Params>
@@ -71,7 +78,5 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
 cudaError_t launch_moe_router(int32_t* ids, float* weights, float* logits, const uint8_t* qs, const uint16_t* d,
                               const float* x, int T, int E, int K, int topk, bool normalize, cudaStream_t s);
 
-// ---- device fault word (set by the MoE kernels on an expert id outside [0, E)) --------------------
-cudaError_t read_and_clear_fault_moe(unsigned* out);
 
 }  // namespace q4

@@ -9,7 +9,8 @@
 // Kernel shape (one persistent CTA of W warps per SM):
 //  * the V input vectors are staged once per CTA in shared memory, block by block: each element is
 //    pre-scaled for the bit position of its code and its block's exponent bound, and beside each block sit
-//    its factor 2^(22+e) and -8 times its sum (device_common.cuh, bias-free decode);
+//    its factor 2^(22+e) and the -8 offset term of the block (q4_block_bias: the unit chain on codes of 8, so
+//    a block of zero weights contributes exactly zero; device_common.cuh, bias-free decode);
 //  * every warp owns a ring of D shared-memory slots; a slot holds R consecutive rows x CB = 32*UPL blocks
 //    (quants, then scales), so each weight byte is read from HBM once and all V vectors use it. Whole rows of
 //    exactly CB blocks travel as two bulk copies (quants, scales) issued by lane 0 on the slot's mbarrier;
@@ -17,10 +18,13 @@
 //  * lane l handles units l, l+32, ... of every row in the slot, in increasing order whatever CB is, so
 //    the per-row summation order depends only on K: batched rows equal single-vector calls bit for bit;
 //  * per 32-bit word: one shift and eight ANDs turn the codes into floats, and four packed fp32x2 FMAs per
-//    vector accumulate against the staged quads; per block: t = A * 2^(22+e) - 8 * sum(x), then d * t;
+//    vector accumulate against the staged quads in the common chain order (word_fma); per block:
+//    t = A * 2^(22+e) + bias, then d * t;
 //  * the per-stage control is incremental (no division in the loop) and full chunks run unguarded;
 //  * at the end of a row group the R*V totals are summed across the warp with a transposing shuffle
-//    reduction and stored.
+//    reduction and stored;
+//  * a stage wait (bulk mode) that runs out of its limit makes the warp stop issuing copies and store its
+//    remaining rows as NaN (kFaultWaitTimeout); before exiting it waits, bounded, for the copies it issued.
 #pragma once
 
 #include <algorithm>
@@ -42,6 +46,8 @@ struct Q4Params {
     int jobs;   // row groups of R rows
     int dcopy;  // scales move by 16-byte copies (else the warp loads them into the slot itself)
     int bulk;   // every stage is whole rows: one bulk copy each for quants and scales, on a slot mbarrier
+    long long wait_cycles;  // limit of one stage wait
+    unsigned* fault;        // device fault word
     uint32_t xs_off, aux_off, bar_off, slots_off;
 };
 
@@ -74,9 +80,6 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     const uint32_t aux = s_base + p.aux_off;
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
     const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot (bulk mode)
-    // set when a stage wait ran out: the CTA's rows are then stored as NaN
-    int& s_err = *reinterpret_cast<int*>(smem + p.bar_off + W * D * 8);
-    if (threadIdx.x == 0) s_err = 0;
     if (p.bulk) {
         if (lane == 0) {
 #pragma unroll
@@ -94,8 +97,10 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     // Issue pointer: the next stage to copy (job, chunk) and its slot. One commit group per call, empty
     // once this warp has no stage left, so the wait below always counts D - 1 groups ahead.
     int ijob = gw, ic = 0, islot = 0;
+    int nissued = 0;        // stages issued (bulk mode)
+    bool aborted = false;   // a stage wait ran out: no more copies, the warp's remaining rows are NaN
     auto issue = [&]() {
-        if (ijob < p.jobs) {
+        if (ijob < p.jobs && !aborted) {
             const int r0 = ijob * R;
             const int rv = min(R, p.N - r0);
             const int b0 = ic * CB;
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                     bulk_copy(slot, p.qs + (size_t)r0 * QROW, (uint32_t)rv * QROW, bar, pol);
                     bulk_copy(slot + QBYTES, p.d + (size_t)r0 * CB, (uint32_t)(rv * CB * 2), bar, pol);
                 }
+                ++nissued;
             } else if (nb == CB && p.S == 1) {
                 warp_copy_async(slot, p.qs + (size_t)r0 * QROW, (uint32_t)rv * QROW, lane, pol);
                 if (p.dcopy)
@@ -183,10 +189,22 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                                  : "memory");
                     if (t4 == 0)
                         asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset((uint32_t)v, u, (uint32_t)V)),
-                                     "f"(block_factor(st.e)), "f"(-8.0f * st.sum)
+                                     "f"(block_factor(st.e)), "f"(0.0f)
                                      : "memory");
                 }
             }
+        }
+        __syncthreads();
+        // each block's -8 offset term: the unit chain on codes of 8 over its staged quads
+        for (int b = threadIdx.x; b < nb_all; b += kThreads) {
+            const int v = b / p.nblk;
+            const uint32_t u = (uint32_t)(b - v * p.nblk);
+            float4 xq[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xq[q] = lds128f(xs + xs_chunk_offset((uint32_t)v, (uint32_t)q, u, (uint32_t)V));
+            const uint32_t a = aux + aux_offset((uint32_t)v, u, (uint32_t)V);
+            const float bias = q4_block_bias(xq, lds32f(a));
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 4u), "f"(bias) : "memory");
         }
     }
     __syncthreads();
@@ -210,11 +228,19 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
     const int total = my_jobs * p.S;
     int job = gw, c = 0, cslot = 0;
     uint32_t cphase = 0u;
+    int consumed = 0;  // stages whose wait completed (bulk mode)
     for (int g = 0; g < total; ++g) {
         issue();  // stage g + D - 1 into the slot consumed at g - 1
         // stage g has landed: its slot's mbarrier completed phase cphase (bounded wait), or its commit group
         if (p.bulk) {
-            if (!mbar_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, kWaitCycles)) s_err = 1;
+            if (!aborted) {
+                if (warp_wait_bounded(bars + 8u * (uint32_t)cslot, cphase, p.wait_cycles)) {
+                    consumed = g + 1;
+                } else {
+                    aborted = true;
+                    if (lane == 0) atomicOr(p.fault, kFaultWaitTimeout);
+                }
+            }
         } else {
             cp_async_wait<D - 1>();
         }
@@ -243,7 +269,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) fold[r] ^= w[r].x ^ w[r].y ^ w[r].z ^ w[r].w ^ dbits[r];
             } else {
-                // one fp32x2 chain per row and vector
+                // one fp32x2 chain per row and vector, in the common word order
                 float2 acc[R][V];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -257,14 +283,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                         const float4 xl = xa[0];
                         const float4 xh = xa[128];
 #pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            float2 a = i == 0 ? make_float2(0.f, 0.f) : acc[r][v];
-                            a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
-                            a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
-                            a = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), a);
-                            a = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), a);
-                            acc[r][v] = a;
-                        }
+                        for (int r = 0; r < R; ++r)
+                            acc[r][v] = word_fma(d8[r], xl, xh, i == 0 ? make_float2(0.f, 0.f) : acc[r][v]);
                     }
                 }
 #pragma unroll
@@ -278,7 +298,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 }
             }
         };
-        if constexpr (R * V <= 2) {
+        if (aborted) {
+            // no compute after a timed-out wait; the rows are stored as NaN below
+        } else if constexpr (R * V <= 2) {
             // short bodies: unrolled, so neighbouring units overlap; full chunks run unguarded
             if (nb == CB) {
 #pragma unroll
@@ -303,8 +325,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 for (int r = 0; r < R; ++r) {
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) fold[r] ^= __shfl_xor_sync(0xffffffffu, fold[r], off);
-                    if (lane == 0 && r < rv)
-                        p.y[r0 + r] = *reinterpret_cast<volatile int*>(&s_err) ? NAN : __uint_as_float(fold[r]);
+                    if (lane == 0 && r < rv) p.y[r0 + r] = aborted ? NAN : __uint_as_float(fold[r]);
                     fold[r] = 0u;
                 }
             } else {
@@ -328,7 +349,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                     const int r = idx / V;
                     const int v = idx - r * V;
                     if (r < rv)
-                        p.y[(size_t)v * p.N + r0 + r] = *reinterpret_cast<volatile int*>(&s_err) ? NAN : vals[0];
+                        p.y[(size_t)v * p.N + r0 + r] = aborted ? NAN : vals[0];
                 }
             }
         }
@@ -341,29 +362,10 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
             cphase ^= 1u;
         }
     }
-}
-
-// Developer switch back to per-lane cp.async copies for whole-row stages, read once from Q4GEMV_Q4_BULK=0.
-inline bool bulk_off() {
-    static bool off = false;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_Q4_BULK");
-        off = e && e[0] == '0';
-    });
-    return off;
-}
-
-// Developer override of the ring depth, read once from Q4GEMV_Q4_DEPTH. Used for tuning sweeps; the
-// defaults in the launchers come from such sweeps.
-inline int depth_override(int d) {
-    static int o = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_Q4_DEPTH");
-        if (e) o = atoi(e);
-    });
-    return o > 0 ? o : d;
+    // bulk copies issued but not consumed (only after a wait ran out): let them land before the CTA exits
+    for (int st = consumed; st < nissued; ++st)
+        if (!warp_wait_bounded(bars + 8u * (uint32_t)(st % D), (uint32_t)((st / D) & 1), kDrainCycles) && lane == 0)
+            atomicOr(p.fault, kFaultCopyLost);
 }
 
 template <int V, int R, int W, int D, int UPL, bool PURE>
@@ -373,7 +375,7 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     const uint32_t nblk = (uint32_t)K / 32u;
     const uint32_t xsb = PURE ? 0u : xs_chunk_bytes((uint32_t)V, nblk);
     const uint32_t axb = PURE ? 0u : aux_bytes((uint32_t)V, nblk);
-    const uint32_t barb = round_up_u((uint32_t)(W * D * 8 + 4), 128u);  // slot mbarriers and the error word
+    const uint32_t barb = round_up_u((uint32_t)(W * D * 8), 128u);  // slot mbarriers
     const uint32_t smem = xsb + axb + barb + (uint32_t)(W * D) * slot_bytes<R, UPL>();
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;
     auto kern = q4_gemv_kernel<V, R, W, D, UPL, PURE>;
@@ -394,7 +396,10 @@ cudaError_t launch_fixed(const DeviceInfo& di, float* y, const uint8_t* qs, cons
     p.S = (int)((nblk + CB - 1) / CB);
     p.jobs = (N + R - 1) / R;
     p.dcopy = dcopy ? 1 : 0;
-    p.bulk = (dcopy && p.S == 1 && (int)nblk == CB && !bulk_off()) ? 1 : 0;
+    p.bulk = (dcopy && p.S == 1 && (int)nblk == CB) ? 1 : 0;
+    p.wait_cycles = wait_limit_cycles();
+    p.fault = device_fault_word(di.device);
+    if (!p.fault) return cudaErrorInvalidSymbol;
     p.xs_off = 0;
     p.aux_off = xsb;
     p.bar_off = xsb + axb;
@@ -429,7 +434,7 @@ cudaError_t launch(const DeviceInfo& di, float* y, const uint8_t* qs, const uint
                    int depth, int upl_max, cudaStream_t s) {
     const int nblk = K / 32;
     const bool dcopy = (nblk % 8 == 0) && ((reinterpret_cast<uintptr_t>(d) & 15u) == 0);
-    depth = std::min(depth_override(depth), DMAX);
+    depth = std::min(depth, DMAX);
     const int upl0 = std::min(nblk <= 32 ? 1 : nblk <= 64 ? 2 : 4, upl_max);
     cudaError_t e = cudaErrorNotSupported;
     if (upl0 == 4) e = launch_upl<V, R, W, DMAX, 4, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
@@ -437,18 +442,6 @@ cudaError_t launch(const DeviceInfo& di, float* y, const uint8_t* qs, const uint
         e = launch_upl<V, R, W, DMAX, 2, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
     if (e == cudaErrorNotSupported) e = launch_upl<V, R, W, DMAX, 1, PURE>(di, y, qs, d, x, N, K, dcopy, depth, s);
     return e;
-}
-
-// Developer override of the batched variant (rows per lane and warps), read once from Q4GEMV_Q4_VB
-// (48: 4 rows x 8 warps; 216: 2 rows x 16 warps; 28: 2 rows x 8 warps). Used for tuning sweeps.
-inline int batched_variant() {
-    static int o = 48;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const char* e = getenv("Q4GEMV_Q4_VB");
-        if (e) o = atoi(e);
-    });
-    return o;
 }
 
 // Per-translation-unit entry points (kernels_q4_*.cu).

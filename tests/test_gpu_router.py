@@ -93,3 +93,39 @@ def test_router_refusals():
     w = torch.empty(2, 9, device="cuda")
     with pytest.raises(q4.Q4Error, match="topk"):
         q4.moe_router_q4(ids, w, cu(qs), cu(d), x, 9, True)
+
+
+def test_router_nan_input_ranks_every_expert_equal_and_last(oracle_lib):
+    # a NaN in token 0's x makes all its logits NaN: NaNs tie to the lower index (ids 0..topk-1) and every
+    # weight is NaN; token 1 is unaffected
+    E, K, T, topk = 32, 512, 2, 5
+    rng = np.random.default_rng(77)
+    qs, d = synth.q4_weights(rng, E, K)
+    x = synth.activations(rng, T, K)
+    x[0, 100] = np.nan
+    ids, w, lg = run_router(qs, d, x, topk, True)
+    assert np.all(np.isnan(lg[0])) and np.all(np.isfinite(lg[1]))
+    assert ids[0].tolist() == list(range(topk))
+    assert np.all(np.isnan(w[0]))
+    own_ids, own_w = oracle_lib.topk_softmax_f32(lg, topk, True)
+    assert np.array_equal(ids, own_ids)
+    assert np.allclose(w[1], own_w[1], rtol=2e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("E", [6, 40, 100])
+def test_router_nan_logit_comes_last_with_topk_all(E, oracle_lib):
+    # one expert's row has a NaN scale, so its logit is NaN; with topk = E it must be the last pick
+    K, T = 256, 3
+    rng = np.random.default_rng(E)
+    qs, d = synth.q4_weights(rng, E, K)
+    bad = E // 3
+    d[bad, 2] = np.float16(np.nan)
+    x = synth.activations(rng, T, K)
+    ids, w, lg = run_router(qs, d, x, E, False)
+    assert np.all(np.isnan(lg[:, bad]))
+    assert np.all(ids[:, -1] == bad)
+    own_ids, _ = oracle_lib.topk_softmax_f32(lg, E, False)
+    assert np.array_equal(ids, own_ids)
+    assert np.all(np.isnan(w)), "a NaN logit makes the softmax NaN"
+    for t in range(T):
+        assert sorted(ids[t].tolist()) == list(range(E))

@@ -13,10 +13,11 @@
 //    warp's ring of D slots (mbarrier per slot, bounded waits). KS is chosen per problem so that the groups
 //    cover the tiles evenly with the fewest stages per warp;
 //  * prologue: one stage per warp is requested, then (after the previous kernel in the stream is done) each
-//    thread loads its eight elements of x (and gamma) once: sum(x^2) for r = rsqrt(sum/K + eps) comes from the
-//    same registers that are then staged as xhat = x * r * gamma, per 32-element sub-block j pre-scaled for the
-//    bias-free decode with its own exponent bound e_j; beside it (S_j, 2^(22+e_j)), where S_j * 2^(-22-e_j) is
-//    the sub-block's FMA chain run on codes of 1, formed by the four lanes of the sub-block through shuffles;
+//    thread loads its eight elements of x and gamma in one round trip: sum(x^2) for r = rsqrt(sum/K + eps)
+//    comes from the same registers that are then staged as x * gamma (r, one scalar for the whole row sum,
+//    multiplies the row totals at the end), per 32-element sub-block j pre-scaled for the bias-free decode
+//    with its own exponent bound e_j; beside it (S_j, 2^(22+e_j)), where S_j * 2^(-22-e_j) is the sub-block's
+//    FMA chain run on codes of 1, formed by the four lanes of the sub-block through shuffles;
 //  * lane l decodes the header of its own row's super-block once: each 6-bit scale or min becomes the float
 //    2^23 + v by one byte permute, and one FMA with d (or dmin) and -d * 2^23 gives d * sc exactly;
 //  * per word: one shift and eight ANDs, then packed fp32x2 FMAs against the staged input (every lane reads
@@ -85,136 +86,143 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
     const int warp = threadIdx.x >> 5;
     const int nthreads = (int)blockDim.x;
     const uint32_t s_base = smem_addr(smem);
-    const uint32_t ring = s_base + p.slots_off + (uint32_t)(warp * D) * kSlot;
-    const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot
+    const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // this warp's mbarriers, one per slot
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < D; ++k) mbar_init(bars + 8u * k, 1u);
+    const int nwarps = nthreads / 32;
+    if ((int)threadIdx.x < nwarps * D) {
+        mbar_init(s_base + p.bar_off + 8u * threadIdx.x, 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncwarp();
+    __syncthreads();
 
-    // group g (tiles gid, gid + G*grid, ...), warp k of it (super-blocks k, k + KS, ... of each tile)
-    const int g = warp / p.KS, k = warp - g * p.KS;
-    const int spw = k < p.nsb ? (p.nsb - 1 - k) / p.KS + 1 : 0;  // stages per tile for this warp
-    const int gid = g * (int)gridDim.x + (int)blockIdx.x, gstep = p.G * (int)gridDim.x;
-    const int my_tiles = gid < p.tiles ? (p.tiles - 1 - gid) / gstep + 1 : 0;
-    const int total = my_tiles * spw;
-
-    // stage j: tile j / spw of this group, super-block k + (j % spw) * KS, into slot j % D
+    // Warp wi belongs to group wi / KS (tiles gid, gid + G*grid, ...) as its warp k = wi % KS (super-blocks k,
+    // k + KS, ... of each tile). Its stage j is tile j / spw of the group, super-block k + (j % spw) * KS, into
+    // slot j % D of the warp's ring.
+    const int gstep = p.G * (int)gridDim.x;
+    struct Plan {
+        int k, spw, gid, tiles, total;
+    };
+    auto plan_of = [&](int wi) {
+        Plan w;
+        const int gi = wi / p.KS;
+        w.k = wi - gi * p.KS;
+        w.spw = w.k < p.nsb ? (p.nsb - 1 - w.k) / p.KS + 1 : 0;  // 0 when KS > nsb: the warp only meets barriers
+        w.gid = gi * (int)gridDim.x + (int)blockIdx.x;
+        w.tiles = w.gid < p.tiles ? (p.tiles - 1 - w.gid) / gstep + 1 : 0;  // the same for every warp of a group
+        w.total = w.tiles * w.spw;
+        return w;
+    };
+    auto issue_for = [&](int wi, const Plan& w, int j) {
+        const int jt = j / w.spw;
+        const int sb = w.k + (j - jt * w.spw) * p.KS;
+        const int r0 = (w.gid + jt * gstep) * TR;
+        const uint32_t bar = s_base + p.bar_off + (uint32_t)(wi * D + j % D) * 8u;
+        const uint32_t dst = s_base + p.slots_off + (uint32_t)(wi * D + j % D) * kSlot;
+        mbar_expect_tx(bar, kSlot);
+        tma_load_2d(dst, &p.tm0, sb * kSB, r0, bar, pol);  // rows past N arrive zero-filled
+        if constexpr (NS == 2) tma_load_2d(dst + (uint32_t)(TR * kSB), &p.tm1, sb * kSB, r0, bar, pol);
+    };
+    const Plan me = plan_of(warp);
+    const int g = warp / p.KS, k = me.k, spw = me.spw, gid = me.gid, total = me.total;
+    const int my_tiles = me.tiles;  // every warp of the group takes part in each tile's barrier
+    // A slot is refilled only after every lane of the warp has read it (the __syncwarp before each refill), and a
+    // proxy fence orders those reads before the tensor copy's writes.
     auto issue = [&](int j) {
         if (lane == 0) {
-            const int jt = j / spw;
-            const int sb = k + (j - jt * spw) * p.KS;
-            const int r0 = (gid + jt * gstep) * TR;
-            const uint32_t bar = bars + 8u * (uint32_t)(j % D);
-            const uint32_t dst = ring + (uint32_t)(j % D) * kSlot;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(bar, kSlot);
-            tma_load_2d(dst, &p.tm0, sb * kSB, r0, bar, pol);  // rows past N arrive zero-filled
-            if constexpr (NS == 2) tma_load_2d(dst + (uint32_t)(TR * kSB), &p.tm1, sb * kSB, r0, bar, pol);
+            issue_for(warp, me, j);
         }
     };
-    int issued = min(1, total);
-    if (issued) issue(0);
+    if (total > 0) issue(0);
 
     // The weights are constant; x, gamma and the outputs may belong to the previous kernel in the stream.
     grid_dependency_wait();
     grid_launch_dependents();
+    // The other slots of every ring are requested by the lanes of the last warp, while the rest stage the input
+    // (a burst of copies from one SM is accepted at a limited rate; spread over the warps it would hold each of
+    // them for that long).
+    if (warp == nwarps - 1 && lane < nwarps) {
+        const Plan w = plan_of(lane);
+        for (int j = 1; j < min(D, w.total); ++j) issue_for(lane, w, j);
+    }
+    int issued = min(D, total);
 
     float* const red = reinterpret_cast<float*>(smem + p.red_off);  // [2][G][KS][32] partials, then [2][G] flags
     int* const red_bad = reinterpret_cast<int*>(red + 2 * kMaxWarps * 32);
+    float* const part = reinterpret_cast<float*>(red_bad + 2 * kMaxWarps);  // one sum of squares per warp
+    float r = 1.0f;  // RMSNorm factor, applied to the row sums
     if constexpr (PURE) {
         if (threadIdx.x < 2 * kMaxWarps) red_bad[threadIdx.x] = 0;
+        __syncthreads();
     } else {
-        // Each thread holds elements 8t .. 8t+7 (t = its lane within a group of four) of sub-block thr / 4 in
-        // registers: loaded once, used for sum(x^2) and then staged (K/32 is a multiple of 8, so every loop
-        // runs whole warps and the group shuffles see 32 lanes).
+        // Each thread holds elements 8t .. 8t+7 (t = its lane within a group of four) of sub-block thr / 4 of x
+        // and gamma in registers, loaded in one round trip: sum(x^2) comes from them and x * gamma is staged
+        // from them. The factor r = rsqrt(sum/K + eps) is a scalar of the whole row sum, so it multiplies the
+        // row results at the end and the staging does not wait for the block-wide sum (K/32 is a multiple of
+        // 8, so every loop runs whole warps and the group shuffles see 32 lanes).
         constexpr int kIt = 4;  // sub-block quarters a thread keeps in registers; longer inputs load twice
         const int nsub = p.K / 32;
         const int iters = (nsub * 4 + nthreads - 1) / nthreads;
         const bool keep = iters <= kIt;
+        const bool norm = p.gamma != nullptr;
         const int t4 = lane & 3;
-        float4 xa[kIt], xb[kIt];
-        auto load_x = [&](int thr, float4& a, float4& b) {
-            const float4* src = reinterpret_cast<const float4*>(p.x) + (thr >> 2) * 8 + 2 * t4;
-            a = __ldg(src);
-            b = __ldg(src + 1);
+        float4 xa[kIt], xb[kIt], ga[kIt], gb[kIt];
+        auto load_xg = [&](int thr, float4& a, float4& b, float4& c, float4& e) {
+            const int q = (thr >> 2) * 8 + 2 * t4;
+            a = __ldg(reinterpret_cast<const float4*>(p.x) + q);
+            b = __ldg(reinterpret_cast<const float4*>(p.x) + q + 1);
+            if (norm) {
+                c = __ldg(reinterpret_cast<const float4*>(p.gamma) + q);
+                e = __ldg(reinterpret_cast<const float4*>(p.gamma) + q + 1);
+            }
         };
-        float r = 1.0f;
+        auto sumsq = [](float ss, float4 a, float4 b) {
+            ss = fmaf(a.x, a.x, ss);
+            ss = fmaf(a.y, a.y, ss);
+            ss = fmaf(a.z, a.z, ss);
+            ss = fmaf(a.w, a.w, ss);
+            ss = fmaf(b.x, b.x, ss);
+            ss = fmaf(b.y, b.y, ss);
+            ss = fmaf(b.z, b.z, ss);
+            return fmaf(b.w, b.w, ss);
+        };
         if (keep) {
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
                 const int thr = (int)threadIdx.x + it * nthreads;
-                if (it < iters && thr < nsub * 4) load_x(thr, xa[it], xb[it]);
+                if (it < iters && thr < nsub * 4) load_xg(thr, xa[it], xb[it], ga[it], gb[it]);
             }
         }
-        if (p.gamma) {
-            float ss = 0.f;
-            if (keep) {
-#pragma unroll
-                for (int it = 0; it < kIt; ++it) {
-                    if (it < iters && (int)threadIdx.x + it * nthreads < nsub * 4) {
-                        ss = fmaf(xa[it].x, xa[it].x, ss);
-                        ss = fmaf(xa[it].y, xa[it].y, ss);
-                        ss = fmaf(xa[it].z, xa[it].z, ss);
-                        ss = fmaf(xa[it].w, xa[it].w, ss);
-                        ss = fmaf(xb[it].x, xb[it].x, ss);
-                        ss = fmaf(xb[it].y, xb[it].y, ss);
-                        ss = fmaf(xb[it].z, xb[it].z, ss);
-                        ss = fmaf(xb[it].w, xb[it].w, ss);
-                    }
-                }
-            } else {
-                for (int thr = threadIdx.x; thr < nsub * 4; thr += nthreads) {
-                    float4 a, b;
-                    load_x(thr, a, b);
-                    ss = fmaf(a.x, a.x, ss);
-                    ss = fmaf(a.y, a.y, ss);
-                    ss = fmaf(a.z, a.z, ss);
-                    ss = fmaf(a.w, a.w, ss);
-                    ss = fmaf(b.x, b.x, ss);
-                    ss = fmaf(b.y, b.y, ss);
-                    ss = fmaf(b.z, b.z, ss);
-                    ss = fmaf(b.w, b.w, ss);
-                }
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            float* const part = reinterpret_cast<float*>(red_bad + 2 * kMaxWarps);  // one sum per warp
-            if (lane == 0) part[warp] = ss;
-            __syncthreads();
-            float tot = 0.f;
-            for (int w = 0; w < nthreads / 32; ++w) tot += part[w];
-            r = rsqrtf(tot / (float)p.K + p.eps);
-        }
-        // xhat staged per sub-block j in element order, pre-scaled for the code positions of the low (j even)
+        // xhat / r staged per sub-block j in element order, pre-scaled for the code positions of the low (j even)
         // or high (j odd) nibbles, and S_j from the chain of the sub-block's quads 0..7 on codes of 1: the four
         // lanes of the group take their two quads in turn, passing the running pair by shuffles.
         float4* const xs = reinterpret_cast<float4*>(smem + p.xs_off);
         float2* const ssum = reinterpret_cast<float2*>(smem + p.ss_off);
         const Word8s c1 = decode_word_sub(0x11111111u);
+        float ss = 0.f;
         for (int it = 0, thr = threadIdx.x; thr < nsub * 4; ++it, thr += nthreads) {
             const int js = thr >> 2;
-            float4 a, b;
+            float4 a, b, c, e;
             if (keep) {
                 a = xa[0];
                 b = xb[0];
+                c = ga[0];
+                e = gb[0];
 #pragma unroll
                 for (int q = 1; q < kIt; ++q)
                     if (it == q) {
                         a = xa[q];
                         b = xb[q];
+                        c = ga[q];
+                        e = gb[q];
                     }
             } else {
-                load_x(thr, a, b);
+                load_xg(thr, a, b, c, e);
             }
-            if (p.gamma) {
-                const float4* gsrc = reinterpret_cast<const float4*>(p.gamma) + js * 8 + 2 * t4;
-                const float4 ga = __ldg(gsrc), gb = __ldg(gsrc + 1);
-                a = make_float4((a.x * r) * ga.x, (a.y * r) * ga.y, (a.z * r) * ga.z, (a.w * r) * ga.w);
-                b = make_float4((b.x * r) * gb.x, (b.y * r) * gb.y, (b.z * r) * gb.z, (b.w * r) * gb.w);
+            if (norm) {
+                ss = sumsq(ss, a, b);
+                a = make_float4(a.x * c.x, a.y * c.y, a.z * c.z, a.w * c.w);
+                b = make_float4(b.x * e.x, b.y * e.y, b.z * e.z, b.w * e.w);
             }
             const int hi = js & 1;
             const Stage4 st = stage_block4(a, b, hi);
@@ -236,9 +244,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
                 ssum[js] = make_float2((acc.x + acc.y) * f, f);
             }
         }
+        if (norm) {
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0) part[warp] = ss;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    for (; issued < min(D, total); ++issued) issue(issued);
 
     bool aborted = false;  // a stage wait ran out: no more copies, this warp's partials are NaN
     int consumed = 0;
@@ -333,8 +345,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) q4k_rows_kernel(const __gri
                 if (lane == 0) red_bad[par * kMaxWarps + g] = 0;
                 if (r0 + rr < p.N) (NS == 2 && lane >= TR ? p.y1 : p.y0)[r0 + rr] = bad ? NAN : __uint_as_float(f);
             } else {
+                if (t == 0 && p.gamma) {  // the RMSNorm factor, from the per-warp sums of squares
+                    float tot = 0.f;
+                    for (int w = 0; w < nwarps; ++w) tot += part[w];
+                    r = rsqrtf(tot / (float)p.K + p.eps);
+                }
                 float v = 0.f;
                 for (int w = 0; w < p.KS; ++w) v += gbuf[w * 32 + lane];
+                v *= r;
                 if (NS == 2 && p.swiglu) {
                     const float up = __shfl_down_sync(0xffffffffu, v, TR);
                     if (lane < TR && r0 + rr < p.N) p.y0[r0 + rr] = silu(v) * up;

@@ -41,7 +41,7 @@ METRIC = "effective weight GB/s per GEMV call and % of GB300 HBM peak; \u00b5s/c
 
 KERNEL_SOURCES = ["device_common.cuh", "launch.h", "q4_dense.cuh", "kernels_q4.cu", "kernels_q4_v2_4.cu",
                   "kernels_q4_v5_8.cu", "kernels_q4_v9_16.cu", "kernels_q4k.cu", "kernels_q4k_rows.cu",
-                  "kernels_q4k_batched.cu", "kernels_moe.cu", "kernels_router.cu"]
+                  "kernels_q4k_batched.cu", "kernels_moe.cu", "kernels_router.cu", "q4_xr.cuh"]
 
 
 # ------------------------------------------------------------------------------------------------
@@ -78,6 +78,13 @@ def call_table(c5_ids):
         ("q4_gemv_batched 14336x4096 M=8", q4_bytes(14336, 4096), "q4_batched_14336x4096_m8"),
         (f"moe_q4_gemv e64 1408x2048 t8k8 ({uniq} experts)", 2 * uniq * q4_bytes(1408, 2048), "moe_q4_e64_t8k8"),
     ]
+
+
+def call_fmas(c5_ids):
+    """fp32 FMAs of each call of a step (M per weight and vector; MoE: every token's slot, gate and up)."""
+    T, topk = np.asarray(c5_ids).shape
+    return [256 * 1024, 3584 * 3584, 2 * 18944 * 3584] + [M * 14336 * 4096 for M in (1, 2, 4, 8)] + \
+        [T * topk * 2 * 1408 * 2048]
 
 
 WORKLOAD_NAME = ("decode GEMV suite: Q4 256x1024; RMSNorm+Q4_K 3584x3584; gate+up Q4_K 2x18944x3584; "
@@ -217,31 +224,57 @@ def aggregate(per_rank_seconds: float, bytes_per_step: float, steps: int, world:
 # CPU oracle leg
 # ------------------------------------------------------------------------------------------------
 
-def oracle_step(o, inputs, frac=1.0):
-    """The step's work on the host oracle, on the first `frac` of each matrix's rows. Returns weight bytes."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def row_chunks(n: int, parts: int):
+    """[lo, hi) ranges that split n rows into at most `parts` nearly equal chunks."""
+    step = -(-n // max(1, parts))
+    return [(lo, min(n, lo + step)) for lo in range(0, n, step)]
+
+
+def oracle_step(o, inputs, frac=1.0, pool=None, parts=1):
+    """The step's work on the host oracle, on the first `frac` of each matrix's rows. Returns weight bytes.
+
+    With a thread pool, every call's rows are split into `parts` chunks that the pool runs at once (the oracle's
+    C functions release the interpreter lock, and a row's result depends only on that row and the inputs)."""
     c1, c2, c3, c4, c5 = inputs
     done = 0
 
     def rows(n):
         return max(1, int(round(n * frac)))
 
+    def run(fn, n):
+        if pool is None:
+            return [fn(0, n)]
+        return list(pool.map(lambda r: fn(*r), row_chunks(n, parts)))
+
     n = rows(256)
-    o.q4_gemv(c1["qs"][:n], c1["d"][:n], c1["x"][0])
+    run(lambda lo, hi: o.q4_gemv(c1["qs"][lo:hi], c1["d"][lo:hi], c1["x"][0]), n)
     done += q4_bytes(n, 1024)
     n = rows(3584)
-    o.fused_rmsnorm_q4k_gemv(c2["w"][:n], c2["x"], c2["gamma"], c2["eps"])
+    run(lambda lo, hi: o.fused_rmsnorm_q4k_gemv(c2["w"][lo:hi], c2["x"], c2["gamma"], c2["eps"]), n)
     done += q4k_bytes(n, 3584)
     n = rows(18944)
-    o.fused_gateup_q4k_gemv(c3["w_gate"][:n], c3["w_up"][:n], c3["x"], c3["gamma"], c3["eps"])
+    run(lambda lo, hi: o.fused_gateup_q4k_gemv(c3["w_gate"][lo:hi], c3["w_up"][lo:hi], c3["x"], c3["gamma"],
+                                               c3["eps"]), n)
     done += 2 * q4k_bytes(n, 3584)
     n = rows(14336)
     for M in (1, 2, 4, 8):
-        o.q4_gemv_batched(c4["qs"][:n], c4["d"][:n], c4["x"][:M])
+        run(lambda lo, hi, M=M: o.q4_gemv_batched(c4["qs"][lo:hi], c4["d"][lo:hi], c4["x"][:M]), n)
         done += q4_bytes(n, 4096)
     n = rows(1408)
-    per_expert = lambda a: np.ascontiguousarray(a.reshape(64, 1408, *a.shape[1:])[:, :n].reshape(64 * n, *a.shape[1:]))  # noqa: E731
-    o.moe_q4_gemv(per_expert(c5["qs_gate"]), per_expert(c5["d_gate"]), per_expert(c5["qs_up"]),
-                  per_expert(c5["d_up"]), c5["x"], c5["ids"], 64)
+
+    def per_expert(a, lo, hi):
+        return np.ascontiguousarray(a.reshape(64, 1408, *a.shape[1:])[:, lo:hi].reshape(64 * (hi - lo), *a.shape[1:]))
+
+    run(lambda lo, hi: o.moe_q4_gemv(per_expert(c5["qs_gate"], lo, hi), per_expert(c5["d_gate"], lo, hi),
+                                     per_expert(c5["qs_up"], lo, hi), per_expert(c5["d_up"], lo, hi), c5["x"],
+                                     c5["ids"], 64), n)
     done += 2 * len(np.unique(c5["ids"])) * q4_bytes(n, 2048)
     return done
 
@@ -252,28 +285,34 @@ def run_reference(args):
         return 0
     import oracle
 
+    from concurrent.futures import ThreadPoolExecutor
+
     o = oracle.default()
     inputs = make_inputs()
-    t0 = time.perf_counter()
-    oracle_step(o, inputs, 1.0 / 64)
-    t_full = (time.perf_counter() - t0) * 64
-    frac = min(1.0 / 16, max(1.0 / 4096, 90.0 / ((args.steps + args.warmup) * t_full)))
-    for _ in range(args.warmup):
-        oracle_step(o, inputs, frac)
-    t0 = time.perf_counter()
-    done = 0
-    for _ in range(args.steps):
-        done += oracle_step(o, inputs, frac)
-    dt = time.perf_counter() - t0
+    cores = host_cores()
+    with ThreadPoolExecutor(cores) as pool:
+        t0 = time.perf_counter()
+        oracle_step(o, inputs, 1.0 / 64, pool, cores)
+        t_full = (time.perf_counter() - t0) * 64
+        frac = min(1.0 / 4, max(1.0 / 4096, 90.0 / ((args.steps + args.warmup) * t_full)))
+        for _ in range(args.warmup):
+            oracle_step(o, inputs, frac, pool, cores)
+        t0 = time.perf_counter()
+        done = 0
+        for _ in range(args.steps):
+            done += oracle_step(o, inputs, frac, pool, cores)
+        dt = time.perf_counter() - t0
     value = done / dt / 1e9
     sample = (f"each step: the suite on the first {frac:.5f} of every matrix's rows (MoE: of every expert's rows), "
-              "sized so that warm-up plus timed steps take about 90 s")
+              f"each call's rows split over {cores} threads; the fraction is sized so that warm-up plus timed steps "
+              f"take about 90 s, at most a quarter of the rows ({(args.steps + args.warmup) * dt / args.steps:.1f} s "
+              "here)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value,
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": WORKLOAD_NAME, "sample": sample},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -433,7 +472,8 @@ def run_gpu(args):
 
     # ---- per-call device time: each call type alone, back to back over weight copies of >= 3x the L2 ------
     peak, peak_kind = measured_peaks()
-    per_call = measure_per_call(suite, inputs, table, stream, peak)
+    fma = measure_fma_ceiling(stream, call_fmas(inputs[4]["ids"])[6])
+    per_call = measure_per_call(suite, inputs, table, stream, peak, fma["fmas_per_us"])
     kt_us = np.array([pc["us"] for pc in per_call])
     dom = int(np.argmax(kt_us))
     traffic = committed_traffic(table[dom][2])
@@ -444,7 +484,9 @@ def run_gpu(args):
                 "algorithmic_bytes": table[dom][1], "us_per_launch": round(float(kt_us[dom]), 3)}
 
     # ---- the NEXT rows (router, SwiGLU forms, wider batches, launch chain), timed the same way ------
-    next_rows = measure_next_rows(suite, inputs, stream, replicas, peak)
+    next_rows = measure_next_rows(suite, inputs, stream, replicas, peak, fma["fmas_per_us"])
+    fma["fmas_per_us"] = round(fma["fmas_per_us"], 1)
+    next_rows["fma_ceiling"] = fma
 
     # ---- end to end through the Python API with host buffers ---------------------------------------
     e2e = run_e2e(suite, inputs, stream, max(20, min(args.steps // 20, 400)), table)
@@ -535,15 +577,38 @@ def _single_us(fn, stream, n=21):
     return float(np.median(ts))
 
 
-def _entry(name, nbytes, us, spread, k, peak, **extra):
+def _entry(name, nbytes, us, spread, k, peak, fmas=None, fma_rate=None, **extra):
+    """One timed call. With its FMA count and the measured FMA rate (FMAs per us, from the FMA-ceiling
+    instrument), the two floors beside it: the weight bytes at the HBM peak and the FMAs at the FMA ceiling,
+    and which of them is the binding roof."""
     e = {"call": name, "us": round(us, 3), "weight_GBps": round(nbytes / us / 1e3, 1),
          "frac_of_hbm_peak": round(nbytes / us / 1e3 / peak, 4), "spread": round(spread, 3),
          "rotation_bytes": int(k * nbytes), "copies": k}
+    if fmas is not None and fma_rate:
+        hbm_floor, fma_floor = nbytes / peak / 1e3, fmas / fma_rate
+        e.update({"hbm_floor_us": round(hbm_floor, 3), "fma_floor_us": round(fma_floor, 3),
+                  "bound": "hbm" if hbm_floor >= fma_floor else "fma",
+                  "frac_of_binding_roof": round(max(hbm_floor, fma_floor) / us, 4)})
     e.update(extra)
     return e
 
 
-def measure_per_call(suite, inputs, table, stream, peak):
+def measure_fma_ceiling(stream, fmas):
+    """The FMA-ceiling instrument at `fmas` FMAs (one launch per call, back to back in a graph): its us, the FMAs
+    it ran and the FMA rate in FMAs per us."""
+    import torch
+
+    import quantized_decode_gemv_q4_gb300 as q4
+
+    sink = torch.empty(1024, device=torch.device("cuda", torch.cuda.current_device()))
+    done = q4.q4_fma_ceiling(sink, fmas, stream=stream)
+    us, sp = _graph_us([lambda: q4.q4_fma_ceiling(sink, fmas, stream=stream)], stream)
+    return {"us": round(us, 3), "spread": round(sp, 3), "fmas": done, "fmas_per_us": done / us,
+            "fp32_TFLOPs": round(2 * done / us / 1e6, 2),
+            "what": "fp32x2 FMA chains on one 512-thread CTA per SM, no loads; the M=8 call's FMA count"}
+
+
+def measure_per_call(suite, inputs, table, stream, peak, fma_rate=None):
     """Each suite call alone, back to back in one CUDA graph over weight copies whose bytes reach 3x the L2, so
     every call streams its weights from HBM; the pure-read instrument of the same bytes beside it."""
     import torch
@@ -553,6 +618,7 @@ def measure_per_call(suite, inputs, table, stream, peak):
     w = suite.sets[0]
     c2eps = float(inputs[1]["eps"])
     c3eps = float(inputs[2]["eps"])
+    fmas = call_fmas(inputs[4]["ids"])
     out = []
 
     def one(j, fns, k, pure=None, pure_per_call=1):
@@ -565,7 +631,7 @@ def measure_per_call(suite, inputs, table, stream, peak):
             extra["pure_read_us"] = round(pus, 3)
             extra["pure_read_frac_of_hbm_peak"] = round(table[j][1] / pus / 1e3 / peak, 4)
             extra["kernel_over_pure_read"] = round(us / pus, 3)
-        out.append(_entry(table[j][0], table[j][1], us, spread, k, peak, **extra))
+        out.append(_entry(table[j][0], table[j][1], us, spread, k, peak, fmas=fmas[j], fma_rate=fma_rate, **extra))
 
     cp, k = cold_copies(w["c1"], table[0][1])
     one(0, [lambda c=c: q4.q4_gemv(suite.y1, c[0], c[1], suite.x1, stream=stream) for c in cp], k)
@@ -594,7 +660,7 @@ def measure_per_call(suite, inputs, table, stream, peak):
     return out
 
 
-def measure_next_rows(suite, inputs, stream, replicas, peak):
+def measure_next_rows(suite, inputs, stream, replicas, peak, fma_rate=None):
     """The router, the SwiGLU forms, the wider batches and a dependent router -> MoE-SwiGLU chain, each over
     weight copies of >= 3x the L2 like the suite's calls."""
     import torch
@@ -632,7 +698,8 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
     for M in (1, 8):
         Yk = torch.empty(M, 18944, device=dev)
         us, sp = _graph_us([lambda m=m: q4.q4k_gemv_batched(Yk, m, Xk[:M], stream=stream) for m in mats], stream)
-        out[f"q4k_gemv_batched 18944x3584 M={M}"] = _entry("", kb, us, sp, len(mats) // 2, peak)
+        out[f"q4k_gemv_batched 18944x3584 M={M}"] = _entry("", kb, us, sp, len(mats) // 2, peak,
+                                                           fmas=M * 18944 * 3584, fma_rate=fma_rate)
     del cp, mats
     uniq = len(np.unique(inputs[4]["ids"]))
     mb = 2 * uniq * q4_bytes(1408, 2048)
@@ -659,7 +726,8 @@ def measure_next_rows(suite, inputs, stream, replicas, peak):
     X16 = torch.from_numpy(np.ascontiguousarray(synth.activations(rng, 16, 2048))).to(dev)
     Y16 = torch.empty(16, 14336, device=dev)
     us, sp = _graph_us([lambda c=c: q4.q4_gemv_batched(Y16, c[0], c[1], X16, stream=stream) for c in cp], stream)
-    out["q4_gemv_batched 14336x2048 M=16"] = _entry("", b16, us, sp, k, peak,
+    out["q4_gemv_batched 14336x2048 M=16"] = _entry("", b16, us, sp, k, peak, fmas=16 * 14336 * 2048,
+                                                    fma_rate=fma_rate,
                                                     fp32_TFLOPs=round(16 * 2 * 14336 * 2048 / us / 1e6, 2))
     del cp
     for v in out.values():
@@ -704,18 +772,35 @@ def run_e2e(suite, inputs, stream, steps, table):
 
 
 def cpu_baseline(inputs):
+    """The oracle on the host: on all cores (each call's rows split over one thread per core), with the
+    single-threaded pass beside it. Each leg runs about 10 s of host work on a row sample of every matrix."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
     o = oracle.default()
-    t0 = time.perf_counter()
-    oracle_step(o, inputs, 1.0 / 64)
-    frac = min(1.0, 10.0 / ((time.perf_counter() - t0) * 64))  # aim at about 10 s of host work
-    t0 = time.perf_counter()
-    done = oracle_step(o, inputs, frac)
-    dt = time.perf_counter() - t0
-    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"one pass of the suite over the first {frac:.3f} of every matrix's rows (MoE: of every "
-                      f"expert's rows); {dt:.1f} s single-threaded fp64"}
+
+    def leg(pool, parts):
+        t0 = time.perf_counter()
+        oracle_step(o, inputs, 1.0 / 64, pool, parts)
+        t_full = (time.perf_counter() - t0) * 64
+        frac = min(1.0, 10.0 / t_full)  # aim at about 10 s of host work: a row sample, or whole passes
+        passes = max(1, int(round(10.0 / t_full))) if frac == 1.0 else 1
+        t0 = time.perf_counter()
+        done = sum(oracle_step(o, inputs, frac, pool, parts) for _ in range(passes))
+        dt = time.perf_counter() - t0
+        return done / dt / 1e9, frac, dt, passes
+
+    cores = host_cores()
+    with ThreadPoolExecutor(cores) as pool:
+        v_all, f_all, t_all, n_all = leg(pool, cores)
+    v_one, f_one, t_one, n_one = leg(None, 1)
+    return {"value": round(v_all, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_all} pass(es) of the suite over the first {f_all:.3f} of every matrix's rows (MoE: of "
+                      f"every expert's rows), each call's rows split over {cores} threads; {t_all:.1f} s fp64",
+            "single_thread": {"value": round(v_one, 4), "cores": 1,
+                              "sample": f"{n_one} pass(es) over the first {f_one:.3f} of every matrix's rows, one "
+                                        f"thread; {t_one:.1f} s"}}
 
 
 CASES = ["c1", "c2", "c3", "c4m1", "c4m2", "c4m4", "c4m8", "c5", "pure_q4", "pure_q4k", "pure_moe"]

@@ -203,6 +203,22 @@ int moe_q4_pure_read(float *sink_gate, float *sink_up, const uint8_t *qs_gate, c
                      int E, int N, int K, int32_t *dev_status, q4_stream_t stream);
 
 /*
+ * FMA-ceiling instrument: at least `fmas` fp32 FMAs (packed fp32x2, a <- a * mul + add in eight independent
+ * chains per thread) on one 512-thread CTA per SM, with no memory traffic but one float per CTA written to
+ * sink. Its time is the floor for a call's FMA work alone: a batched call at M vectors does M FMAs per weight,
+ * and at M = 8 the FMA pipe rather than HBM may bind.
+ * Source: no page defines this instrument; it applies the idea of inferencelayer kernel_lab.rs's `pure_read`
+ * probe (time one resource alone, here the FMA pipe instead of the weight stream).
+ *   sink float[sink_len], sink_len >= the device's SM count; sink[b] = the sum of CTA b's chain ends.
+ *   fmas >= 1; the FMAs run are rounded up to a whole number of rounds (SM count * 512 threads * 16), and the
+ *   count run is stored in *fmas_done when fmas_done is not NULL (host pointer).
+ *   With mul = 1 and add = 0 every chain keeps its start value: thread t's chains j = 0..7 start at
+ *   ((t % 7) + j, (t % 5) + j), so sink[b] is the sum of those 8192 small integers (exact).
+ */
+int q4_fma_ceiling(float *sink, int sink_len, long long fmas, float mul, float add, long long *fmas_done,
+                   q4_stream_t stream);
+
+/*
  * Dequant dumps (debug): W[n][k] = the fp32 weight, bit-exact with the format definitions above
  * ((q - 8) * d for Q4; d*sc*q - dmin*m rounded once to fp32 for Q4_K).
  *   W float[N][K] (16-byte aligned); other arguments as q4_gemv / fused_rmsnorm_q4k_gemv.

@@ -21,7 +21,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "Q4Error", "load", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
+    "Q4Error", "load", "q4_fma_ceiling", "q4_gemv", "q4_gemv_batched", "fused_rmsnorm_q4k_gemv", "fused_gateup_q4k_gemv",
     "moe_q4_gemv", "q4k_gemv_batched", "fused_gateup_swiglu_q4k_gemv", "moe_q4_swiglu_gemv", "moe_router_q4", "q4_pure_read",
     "q4k_pure_read",
     "moe_q4_pure_read", "q4_dequant", "q4k_dequant",
@@ -63,6 +63,8 @@ _SIGNATURES = {
     "moe_router_q4": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "q4k_gemv_batched": [_P, _P, _P, _I, _I, _I, _P],
     "q4_device_faults": [ctypes.POINTER(ctypes.c_uint)],
+    "q4_fma_ceiling": [_P, _I, ctypes.c_longlong, ctypes.c_float, ctypes.c_float, ctypes.POINTER(ctypes.c_longlong),
+                       _P],
 }
 
 
@@ -245,6 +247,14 @@ def q4_pure_read(sink, qs, d, stream=None) -> None:
     N, K = _q4_dims(qs, d)
     _check(load().q4_pure_read(_ptr(sink, torch.float32, "sink"), _ptr(qs, torch.uint8, "qs"),
                                _ptr(d, torch.float16, "d"), N, K, _stream(stream)))
+
+
+def q4_fma_ceiling(sink, fmas: int, mul: float = 1.0 - 2.0 ** -20, add: float = 2.0 ** -20, stream=None) -> int:
+    """Run at least `fmas` fp32 FMAs with no loads (the FMA-ceiling instrument); returns the count run."""
+    done = ctypes.c_longlong(0)
+    _check(load().q4_fma_ceiling(_ptr(sink, torch.float32, "sink"), sink.numel(), int(fmas), float(mul), float(add),
+                                 ctypes.byref(done), _stream(stream)))
+    return done.value
 
 
 def q4k_pure_read(sink, w, stream=None) -> None:

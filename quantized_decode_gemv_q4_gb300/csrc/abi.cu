@@ -319,6 +319,22 @@ int moe_q4_pure_read(float* sink_gate, float* sink_up, const uint8_t* qs_gate, c
                                            topk, E, N, K, dev_status, true, false, (cudaStream_t)stream));
 }
 
+int q4_fma_ceiling(float* sink, int sink_len, long long fmas, float mul, float add, long long* fmas_done,
+                   q4_stream_t stream) {
+    const char* what = "q4_fma_ceiling";
+    Q4_TRY(check_out(what, sink));
+    if (fmas <= 0) return fail(Q4_EINVAL, "%s: fmas must be >= 1 (got %lld)", what, fmas);
+    DeviceInfo di;
+    Q4_TRY(check_device(what, &di));
+    if (sink_len < di.sm_count)
+        return fail(Q4_EINVAL, "%s: sink holds %d floats, the launch writes one per SM (%d)", what, sink_len,
+                    di.sm_count);
+    const long long per = fma_ceiling_fmas_per_iter(di.sm_count);
+    const long long iters = (fmas + per - 1) / per;
+    if (fmas_done) *fmas_done = iters * per;
+    return finish(what, launch_fma_ceiling(sink, iters, mul, add, di.sm_count, (cudaStream_t)stream));
+}
+
 int q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, q4_stream_t stream) {
     const char* what = "q4_dequant";
     Q4_TRY(check_out(what, W, 16));

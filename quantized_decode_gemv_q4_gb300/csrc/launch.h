@@ -50,6 +50,10 @@ cudaError_t launch_kernel(Kernel kern, int grid, int block, uint32_t smem, cudaS
 cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V, int N, int K,
                            cudaStream_t s);
 // Same bytes, same addressing, no math: sink[n] = XOR of row n's quant words and (zero-extended) scales.
+// FMA-ceiling instrument (kernels_probe.cu): `iters` rounds of 16 fp32 FMAs per thread on one 512-thread CTA per
+// SM; fma_ceiling_fmas_per_iter(sm_count) FMAs per round in all.
+long long fma_ceiling_fmas_per_iter(int sm_count);
+cudaError_t launch_fma_ceiling(float* sink, long long iters, float mul, float add, int sm_count, cudaStream_t s);
 cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 cudaError_t launch_q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 

@@ -19,12 +19,12 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
-    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
-    assert line["steps"] == 2 and line["warmup"] == 3
     sys.path.insert(0, ROOT)
     import bench
 
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["steps"] == 2 and line["warmup"] == 3
     assert line["metric"] == bench.METRIC  # the GPU arm prints the same metric string
 
 
@@ -43,6 +43,38 @@ def test_packed_views_are_aligned_and_hold_the_arrays():
         assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
         assert tuple(v.shape) == a.shape and np.array_equal(v.numpy(), a)
     assert buf.numel() == 3 * 256
+
+
+@pytest.mark.parametrize("n,parts", [(1, 4), (7, 3), (18944, 16), (5, 8), (64, 1)])
+def test_row_chunks_cover_the_rows_once(n, parts):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    ch = bench.row_chunks(n, parts)
+    assert len(ch) <= parts and ch[0][0] == 0 and ch[-1][1] == n
+    assert all(lo < hi for lo, hi in ch) and all(a[1] == b[0] for a, b in zip(ch, ch[1:]))
+
+
+def test_oracle_on_row_chunks_equals_the_whole(oracle_lib):
+    """The multithreaded host leg splits every call's rows over threads: the oracle's rows are independent, so
+    the chunks' results side by side are the whole call's, bit for bit."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+
+    g = synth.make_gateup(3, 70, 512)
+    whole = oracle_lib.fused_gateup_q4k_gemv(g["w_gate"], g["w_up"], g["x"], g["gamma"], 1e-5)
+    with ThreadPoolExecutor(4) as pool:
+        parts = list(pool.map(lambda r: oracle_lib.fused_gateup_q4k_gemv(g["w_gate"][r[0]:r[1]], g["w_up"][r[0]:r[1]],
+                                                                         g["x"], g["gamma"], 1e-5),
+                              bench.row_chunks(70, 4)))
+    for s in range(2):
+        for k in range(2):
+            assert np.array_equal(np.concatenate([p[s][k] for p in parts]), whole[s][k])
 
 
 def test_warmup_below_three_is_refused():

@@ -803,7 +803,8 @@ def cpu_baseline(inputs):
                                         f"thread; {t_one:.1f} s"}}
 
 
-CASES = ["c1", "c2", "c3", "c4m1", "c4m2", "c4m4", "c4m8", "c5", "pure_q4", "pure_q4k", "pure_moe"]
+CASES = ["c1", "c2", "c3", "c4m1", "c4m2", "c4m4", "c4m8", "c5", "pure_q4", "pure_q4k", "pure_moe", "router",
+         "c3_swiglu", "c5_swiglu", "q4k_batched_m1", "q4k_batched_m8", "c4m16", "fma"]
 
 
 def run_case(args):
@@ -817,11 +818,50 @@ def run_case(args):
     suite = Suite(inputs, 1, torch.device("cuda", 0))
     fns = suite.calls(0)
     w = suite.sets[0]
-    pick = {"c1": fns[0], "c2": fns[1], "c3": fns[2], "c4m1": fns[3], "c4m2": fns[4], "c4m4": fns[5],
-            "c4m8": fns[6], "c5": fns[7],
-            "pure_q4": lambda: q4.q4_pure_read(suite.Y4[3][0], w["c4"][0][0], w["c4"][0][1]),
-            "pure_q4k": lambda: q4.q4k_pure_read(suite.y3g, w["c3"][0]),
-            "pure_moe": lambda: q4.moe_q4_pure_read(suite.y5g, suite.y5u, *w["c5"], suite.ids5, 64)}[args.case]
+    dev = suite.x1.device
+    rng = np.random.default_rng(7)
+
+    def on_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def router():  # 64 experts x 2048, the MoE tokens, top-8
+        rq, rd = synth.q4_weights(rng, 64, 2048)
+        rq, rd = on_dev(rq), on_dev(rd)
+        ids = torch.empty(8, 8, dtype=torch.int32, device=dev)
+        wts = torch.empty(8, 8, device=dev)
+        return lambda: q4.moe_router_q4(ids, wts, rq, rd, suite.x5, 8, True)
+
+    def q4k_batched(M):  # the gate matrix of the gate+up workload at M vectors
+        X = on_dev(synth.activations(rng, M, 3584))
+        Y = torch.empty(M, 18944, device=dev)
+        return lambda: q4.q4k_gemv_batched(Y, w["c3"][0], X)
+
+    def c4m16():  # 14336 x 2048 at 16 vectors
+        qs, d = synth.q4_weights(rng, 14336, 2048)
+        qs, d = on_dev(qs), on_dev(d)
+        X = on_dev(synth.activations(rng, 16, 2048))
+        Y = torch.empty(16, 14336, device=dev)
+        return lambda: q4.q4_gemv_batched(Y, qs, d, X)
+
+    def fma():  # the FMA-ceiling instrument at the M=8 call's FMA count
+        sink = torch.empty(1024, device=dev)
+        return lambda: q4.q4_fma_ceiling(sink, 8 * 14336 * 4096)
+
+    ysw = torch.empty(18944, device=dev)
+    ymo = torch.empty(8, 8, 1408, device=dev)
+    c3eps = float(inputs[2]["eps"])
+    makers = {"c1": lambda: fns[0], "c2": lambda: fns[1], "c3": lambda: fns[2], "c4m1": lambda: fns[3],
+              "c4m2": lambda: fns[4], "c4m4": lambda: fns[5], "c4m8": lambda: fns[6], "c5": lambda: fns[7],
+              "pure_q4": lambda: lambda: q4.q4_pure_read(suite.Y4[3][0], w["c4"][0][0], w["c4"][0][1]),
+              "pure_q4k": lambda: lambda: q4.q4k_pure_read(suite.y3g, w["c3"][0]),
+              "pure_moe": lambda: lambda: q4.moe_q4_pure_read(suite.y5g, suite.y5u, *w["c5"], suite.ids5, 64),
+              "router": router,
+              "c3_swiglu": lambda: lambda: q4.fused_gateup_swiglu_q4k_gemv(ysw, w["c3"][0], w["c3"][1], suite.x3,
+                                                                            suite.g3, c3eps),
+              "c5_swiglu": lambda: lambda: q4.moe_q4_swiglu_gemv(ymo, *w["c5"], suite.x5, suite.ids5, 64),
+              "q4k_batched_m1": lambda: q4k_batched(1), "q4k_batched_m8": lambda: q4k_batched(8),
+              "c4m16": c4m16, "fma": fma}
+    pick = makers[args.case]()
     for _ in range(args.iters):
         pick()
     torch.cuda.synchronize()

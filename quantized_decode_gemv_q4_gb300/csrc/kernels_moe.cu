@@ -703,23 +703,25 @@ cudaError_t launch_moe_q4_gemv(float* y_gate, float* y_up, const uint8_t* qs_gat
     p.fault = device_fault_word(di.device);
     p.wait_cycles = wait_limit_cycles();
     if (!p.fault) return cudaErrorInvalidSymbol;
-    // plans from sweeps over routing seeds: 16 warps x 4 rows, ring depth 2, contiguous cost-balanced job
-    // ranges; the SwiGLU form (4 gate + 4 up rows per slot) 8 warps with round-robin dealing
+    // plans from sweeps over routing seeds and launch shapes: 8 warps x 8 rows per stage (a staged input quad
+    // serves 8 rows; 16 warps x 4 rows needs more than the 128 registers a 512-thread CTA allows per thread),
+    // ring depth 2, contiguous cost-balanced job ranges; the SwiGLU form (4 gate + 4 up rows per slot) 8 warps
+    // with round-robin dealing
     const int depth = 2;
     p.cost_a = 9;
     p.cost_b = 5;
     p.deal = swiglu ? 1 : 0;
-    // 16 warps x 4 rows when it fits beside the staged tokens, else 8 warps x 4 rows (the same for the pure
-    // read, which streams like the GEMV plan)
-    if (pure_read) {
-        e = launch<4, 16, true>(di, p, depth, s);
-        return e == cudaErrorNotSupported ? launch<4, 8, true>(di, p, depth, s) : e;
-    }
+    // 8 warps x 8 rows when the ring fits beside the staged tokens, else 8 warps x 4 rows; the pure read
+    // streams with the same plan
     if (swiglu) {  // R gate + R up rows per slot
         e = launch<4, 8, false, true>(di, p, depth, s);
         return e == cudaErrorNotSupported ? launch<2, 8, false, true>(di, p, depth, s) : e;
     }
-    e = launch<4, 16, false>(di, p, depth, s);
+    if (pure_read) {
+        e = launch<8, 8, true>(di, p, depth, s);
+        return e == cudaErrorNotSupported ? launch<4, 8, true>(di, p, depth, s) : e;
+    }
+    e = launch<8, 8, false>(di, p, depth, s);
     return e == cudaErrorNotSupported ? launch<4, 8, false>(di, p, depth, s) : e;
 }
 

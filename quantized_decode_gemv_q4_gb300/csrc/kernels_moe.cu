@@ -16,7 +16,7 @@
 //    control, and each selected expert's bytes are read once per call (once per group when more than kMaxC
 //    slots route to one expert);
 //  * all T input vectors are staged once per CTA, block by block, with the bias-free decode's per-block
-//    scaling (device_common.cuh): float4[K/32 blocks / 32][T][8 quads][32] and (2^(22+e), -8 offset term)
+//    scaling (device_common.cuh): float4[K/32 blocks / 32][T][8 quads][32 + 1 pad] and (2^(22+e), -8 offset term)
 //    pairs float2[K/32 / 32][T][32] (the offset term is the unit chain on codes of 8, q4_block_bias, so zero
 //    weights contribute exactly zero), and a lane's quads of a token sit at constant offsets from one base;
 //  * a job's slot count C (1..kMaxC) selects a compiled variant of the stage body, so each decoded code
@@ -40,6 +40,9 @@ namespace q4 {
 namespace {
 
 constexpr int kMaxC = 4;        // routed slots served per weight sweep
+// Grouped staging: a quad row holds the 32 blocks of a group and one 16-byte pad, so the four lanes that stage a
+// block (quads 2t and 2t+1, rows 2t apart) store into distinct bank groups.
+constexpr int kXGRow = 33;      // float4 per quad row
 
 struct MoEParams {
     float* yg;
@@ -403,13 +406,13 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             if (in) {
                 const int v = blk / U;
                 const int u = blk - v * U;
-                // XG layout: [group of 32 blocks][token][quad][block in group]; otherwise [token][quad][block]
+                // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise [token][quad][block]
                 // (16 bytes each): the lanes of a warp read consecutive 16-byte pieces either way
                 const int grp32 = u >> 5, ul = u & 31;
                 const int q0 = 2 * t4;
-                const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * 32 + ul) * 16
+                const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
                                                        : ((v * 8 + q0) * U + u) * 16);
-                const uint32_t qstep = XG ? 512u : (uint32_t)U * 16u;
+                const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
                 asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
                              "f"(st.a.z), "f"(st.a.w)
                              : "memory");
@@ -429,8 +432,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             const int v = b / U;
             const int u = b - v * U;
             const int grp32 = u >> 5, ul = u & 31;
-            const uint32_t q0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8) * 32 + ul) * 16 : ((v * 8) * U + u) * 16);
-            const uint32_t qstep = XG ? 512u : (uint32_t)U * 16u;
+            const uint32_t q0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8) * kXGRow + ul) * 16 : ((v * 8) * U + u) * 16);
+            const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
             float4 xq[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) xq[q] = lds128f(q0 + (uint32_t)q * qstep);
@@ -489,8 +492,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             // blocks of that token (x_it, a_it: the step to the next group)
             const float4* xq[C];
             const float2* aq[C];
-            const int qs = XG ? 32 : U;  // quad stride (float4)
-            const int x_it = XG ? p.T * 8 * 32 : 32, a_it = XG ? p.T * 32 : 32;
+            const int qs = XG ? kXGRow : U;  // quad stride (float4)
+            const int x_it = XG ? p.T * 8 * kXGRow : 32, a_it = XG ? p.T * 32 : 32;
             (void)qs;  // the pure read uses none of these
             (void)x_it;
             (void)a_it;
@@ -498,7 +501,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             for (int m = 0; m < C; ++m) {
                 const int tok = ltok[first + m];
                 xq[m] = reinterpret_cast<const float4*>(smem + p.xs_off) +
-                        (XG ? ((b0 >> 5) * p.T + tok) * 8 * 32 + lane : tok * 8 * U + b0 + lane);
+                        (XG ? ((b0 >> 5) * p.T + tok) * 8 * kXGRow + lane : tok * 8 * U + b0 + lane);
                 aq[m] = reinterpret_cast<const float2*>(smem + p.aux_off) +
                         (XG ? ((b0 >> 5) * p.T + tok) * 32 + lane : tok * U + b0 + lane);
             }
@@ -635,7 +638,7 @@ cudaError_t launch_kernel_cfg(const DeviceInfo& di, const MoEParams& p, uint32_t
 template <int R, int W, int D, int UPL, bool PURE, bool SWIGLU>
 cudaError_t launch_fixed(const DeviceInfo& di, MoEParams p, cudaStream_t s) {
     const uint32_t route = (uint32_t)round_up(route_ints(p.ms) * 4, 128);
-    const uint32_t xsb = PURE ? 0u : (uint32_t)round_up(p.T * p.K * 4, 128);
+    const uint32_t xsb = PURE ? 0u : (uint32_t)round_up(p.T * p.K / 32 * kXGRow * 4 + 512, 128);  // either layout
     const uint32_t axb = PURE ? 0u : (uint32_t)round_up(p.T * p.nblk * 8, 128);
     p.route_off = 0;
     p.xs_off = route;

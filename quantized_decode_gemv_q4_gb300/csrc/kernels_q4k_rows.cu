@@ -37,7 +37,6 @@
 #include <cstdlib>
 #include <mutex>
 
-#include <cuda.h>  // tensor-map types (the encoder is reached through the runtime's driver entry point)
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -383,64 +382,9 @@ cudaError_t launch_rows_fixed(const DeviceInfo& di, const RowParams& p, int nw, 
     return launch_kernel(kern, grid, nw * 32, smem, s, p);
 }
 
-// Tensor map of a Q4_K weight matrix as a 2-D byte tensor [N][K/256*144], box 144 bytes x `rows`, rows past
-// N zero-filled. The encoder comes from the driver through the runtime's entry-point query; maps are cached
-// per (matrix, N, K, rows) since encoding one costs host time on every call otherwise.
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-struct MapEntry {
-    const void* w = nullptr;
-    int N = 0, K = 0, rows = 0;
-    CUtensorMap map;
-};
-
+// Tensor map of a Q4_K weight matrix as a 2-D byte tensor [N][K/256*144], box 144 bytes x `rows`.
 bool weight_map(CUtensorMap* out, const uint8_t* w, int N, int K, int rows) {
-    static std::mutex mu;
-    static MapEntry cache[16];
-    static int next = 0;
-    std::lock_guard<std::mutex> lock(mu);
-    for (const MapEntry& m : cache)
-        if (m.w == w && m.N == N && m.K == K && m.rows == rows) {
-            *out = m.map;
-            return true;
-        }
-    const EncodeTiledFn fn = encode_tiled();
-    if (!fn) return false;
-    const cuuint64_t row_bytes = (cuuint64_t)(K / 256) * kSB;
-    const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)kSB, (cuuint32_t)rows};
-    const cuuint32_t estr[2] = {1u, 1u};
-    MapEntry& e = cache[next];
-    if (fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-        e.w = nullptr;
-        return false;
-    }
-    e.w = w;
-    e.N = N;
-    e.K = K;
-    e.rows = rows;
-    *out = e.map;
-    next = (next + 1) % 16;
-    return true;
+    return cached_tensor_map_2d(out, w, (uint64_t)(K / 256) * kSB, (uint64_t)N, (uint32_t)kSB, (uint32_t)rows, false);
 }
 
 // Shared memory: [staged xhat K*4][(S_j, 2^(22+e_j)) per sub-block][partials 2*16*32 floats, flags, per-warp
@@ -495,6 +439,68 @@ cudaError_t run_rows(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1,
 }
 
 }  // namespace
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The encoder comes from the driver through the runtime's entry-point query.
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+bool cached_tensor_map_2d(CUtensorMap* out, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                          uint32_t box_rows, bool swizzle128) {
+    struct Entry {
+        const void* base = nullptr;
+        uint64_t row_bytes = 0, rows = 0;
+        uint32_t box_bytes = 0, box_rows = 0;
+        bool swz = false;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& m : cache)
+        if (m.base == base && m.row_bytes == row_bytes && m.rows == rows && m.box_bytes == box_bytes &&
+            m.box_rows == box_rows && m.swz == swizzle128) {
+            *out = m.map;
+            return true;
+        }
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    Entry& e = cache[next];
+    if (fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        e.base = nullptr;
+        return false;
+    }
+    e.base = base;
+    e.row_bytes = row_bytes;
+    e.rows = rows;
+    e.box_bytes = box_bytes;
+    e.box_rows = box_rows;
+    e.swz = swizzle128;
+    *out = e.map;
+    next = (next + 1) % 32;
+    return true;
+}
 
 cudaError_t launch_q4k_rows_gemv(float* y0, float* y1, const uint8_t* w0, const uint8_t* w1, const float* x,
                                  const float* gamma, float eps, int N, int K, bool swiglu, cudaStream_t s) {

@@ -2,6 +2,7 @@
 // Arguments reaching these functions have already been validated by the ABI layer.
 #pragma once
 
+#include <cuda.h>  // tensor-map types (the encoder is reached through the runtime's driver entry point)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,6 +28,13 @@ long long wait_limit_cycles();
 // when it cannot be resolved. The word is read and cleared by q4_device_faults.
 unsigned* device_fault_word(int device);
 
+// A 2-D tensor map of a byte matrix [rows][row_bytes] (row_bytes a multiple of 16, base 16-byte aligned), box
+// box_bytes x box_rows, rows past the end read as zero; swizzle128 selects the 128-byte swizzle (box_bytes must
+// then be 128, and the shared-memory destination 1024-byte aligned). Maps are cached per (base, shape, box,
+// swizzle), since encoding one costs host time. False when the driver's encoder is unavailable or refuses.
+bool cached_tensor_map_2d(CUtensorMap* out, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                          uint32_t box_rows, bool swizzle128);
+
 // Launch a GEMV kernel; with launch overlap on, it may start while the previous kernel in the stream is
 // still running (the kernel waits for it before touching inputs or outputs, see grid_dependency_wait).
 template <typename Kernel, typename Params>
@@ -50,11 +58,11 @@ cudaError_t launch_kernel(Kernel kern, int grid, int block, uint32_t smem, cudaS
 cudaError_t launch_q4_gemv(float* Y, const uint8_t* qs, const uint16_t* d, const float* X, int V, int N, int K,
                            cudaStream_t s);
 // Same bytes, same addressing, no math: sink[n] = XOR of row n's quant words and (zero-extended) scales.
+cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 // FMA-ceiling instrument (kernels_probe.cu): `iters` rounds of 16 fp32 FMAs per thread on one 512-thread CTA per
 // SM; fma_ceiling_fmas_per_iter(sm_count) FMAs per round in all.
 long long fma_ceiling_fmas_per_iter(int sm_count);
 cudaError_t launch_fma_ceiling(float* sink, long long iters, float mul, float add, int sm_count, cudaStream_t s);
-cudaError_t launch_q4_pure_read(float* sink, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 cudaError_t launch_q4_dequant(float* W, const uint8_t* qs, const uint16_t* d, int N, int K, cudaStream_t s);
 
 // ---- Q4_K (144-byte super-blocks of 256 weights) ------------------------------------------------------

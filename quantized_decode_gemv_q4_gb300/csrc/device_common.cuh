@@ -258,14 +258,16 @@ __device__ __forceinline__ Stage4 stage_block4(float4 a, float4 b, int hi) {
 }
 
 
-// Chunk-major staged input: float[ceil(U/32)][V][8 quads][32 unit lanes][4] for V vectors of U units. A
+// Chunk-major staged input: float[ceil(U/32)][V][8 quads][32 unit lanes + 1 pad][4] for V vectors of U units. A
 // lane that always works on units u = 32c + lane finds every quad of every vector at one base register plus
-// compile-time offsets, and a warp's 32 lanes read 512 consecutive bytes.
+// compile-time offsets, and a warp's 32 lanes read 512 consecutive bytes. The 16-byte pad after each quad row
+// puts the staging stores of a unit's four lanes (quads 2t and 2t+1) into distinct bank groups.
+constexpr uint32_t kXRow = 33;  // float4 per quad row
 __host__ __device__ __forceinline__ uint32_t xs_chunk_offset(uint32_t v, uint32_t q, uint32_t u, uint32_t V) {
-    return (((u >> 5) * V + v) * 8u + q) * 512u + (u & 31u) * 16u;
+    return (((u >> 5) * V + v) * 8u + q) * (kXRow * 16u) + (u & 31u) * 16u;
 }
 __host__ __device__ __forceinline__ uint32_t xs_chunk_bytes(uint32_t V, uint32_t U) {
-    return ((U + 31u) / 32u) * V * 4096u;
+    return ((U + 31u) / 32u) * V * 8u * kXRow * 16u;
 }
 // Per-block (2^(22+e), -8 * block sum) pairs in the same order: float2[ceil(U/32)][V][32].
 __host__ __device__ __forceinline__ uint32_t aux_offset(uint32_t v, uint32_t u, uint32_t V) {

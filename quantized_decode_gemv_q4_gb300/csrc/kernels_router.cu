@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
                 asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y), "f"(st.a.z),
                              "f"(st.a.w)
                              : "memory");
-                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 512u), "f"(st.b.x), "f"(st.b.y),
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + kXRow * 16u), "f"(st.b.x), "f"(st.b.y),
                              "f"(st.b.z), "f"(st.b.w)
                              : "memory");
                 if (t4 == 0)
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const Word8s d8 = decode_word_sub(i == 0 ? w[j].x : i == 1 ? w[j].y : i == 2 ? w[j].z : w[j].w);
-                    const float4 xl = lds128f(xa + (uint32_t)i * 512u);
-                    const float4 xh = lds128f(xa + (uint32_t)(4 + i) * 512u);
+                    const float4 xl = lds128f(xa + (uint32_t)i * (kXRow * 16u));
+                    const float4 xh = lds128f(xa + (uint32_t)(4 + i) * (kXRow * 16u));
                     acc = word_fma(d8, xl, xh, acc);
                 }
                 const float2 fa = lds64f(aux + aux_offset(0u, (uint32_t)u, 1u));

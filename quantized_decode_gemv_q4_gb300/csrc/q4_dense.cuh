@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
                                  "f"(st.a.z), "f"(st.a.w)
                                  : "memory");
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 512u), "f"(st.b.x), "f"(st.b.y),
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + kXRow * 16u), "f"(st.b.x), "f"(st.b.y),
                                  "f"(st.b.z), "f"(st.b.w)
                                  : "memory");
                     if (t4 == 0)
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
         const int nb = min(CB, p.nblk - b0);
         const uint4* const qb = reinterpret_cast<const uint4*>(slot_p) + lane;
         const uint16_t* const db = reinterpret_cast<const uint16_t*>(slot_p + QBYTES) + lane;
-        const float4* const xb = xs_p + (b0 >> 5) * (V * 256);
+        const float4* const xb = xs_p + (b0 >> 5) * (V * 8 * (int)kXRow);
         const float2* const ab = aux_p + (b0 >> 5) * (V * 32);
 
         auto unit = [&](const int it) {
@@ -279,9 +279,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                         d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const float4* const xa = xb + (it * V + v) * 256 + i * 32;
+                        const float4* const xa = xb + (it * V + v) * (8 * (int)kXRow) + i * (int)kXRow;
                         const float4 xl = xa[0];
-                        const float4 xh = xa[128];
+                        const float4 xh = xa[4 * (int)kXRow];
 #pragma unroll
                         for (int r = 0; r < R; ++r)
                             acc[r][v] = word_fma(d8[r], xl, xh, i == 0 ? make_float2(0.f, 0.f) : acc[r][v]);

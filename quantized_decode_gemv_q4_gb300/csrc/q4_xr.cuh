@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_xr_kernel(const XrParams p) {
 
     if constexpr (!PURE) {
         // Stage x: four lanes per 32-element block (lane t of a group holds elements 8t .. 8t+7), quads stored
-        // lane-major per unit (float4 [UPL][8][32]) so that each lane's register loads are conflict-free. Every
-        // thread issues all of its loads before using any, so staging costs one round trip to the L2.
+        // lane-major per unit (float4 [UPL][8][32 + 1 pad], the rows of the chunk-major layout) so that each
+        // lane's register loads and the four lanes' stores are conflict-free. Every thread issues all of its
+        // loads before using any, so staging costs one round trip to the L2.
         float4* const xs = reinterpret_cast<float4*>(smem + p.xs_off);
         float* const fs = reinterpret_cast<float*>(smem + p.fac_off);
         constexpr int kIter = (32 * UPL * 4 + W * 32 - 1) / (W * 32);  // block-quarters per thread
@@ -125,9 +126,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_xr_kernel(const XrParams p) {
             const int blk = ((int)threadIdx.x + j * W * 32) >> 2;
             const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);  // every lane takes part in the shuffles
             if (blk < p.nblk) {
-                float4* q = xs + ((blk >> 5) * 8 + 2 * t4) * 32 + (blk & 31);
+                float4* q = xs + ((blk >> 5) * 8 + 2 * t4) * kXRow + (blk & 31);
                 q[0] = st.a;
-                q[32] = st.b;
+                q[kXRow] = st.b;
                 if (t4 == 0) fs[blk] = block_factor(st.e);
             }
         }
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_xr_kernel(const XrParams p) {
             const float4* const xs = reinterpret_cast<const float4*>(smem + p.xs_off);
             const bool in = FULL || i * 32 + lane < p.nblk;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) xr[i][q] = in ? xs[(i * 8 + q) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = 0; q < 8; ++q) xr[i][q] = in ? xs[(i * 8 + q) * kXRow + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
             fac[i] = in ? reinterpret_cast<const float*>(smem + p.fac_off)[i * 32 + lane] : 1.0f;
             bias[i] = in ? q4_block_bias(xr[i], fac[i]) : 0.0f;
         }
@@ -274,7 +275,7 @@ cudaError_t launch_xr(const DeviceInfo& di, float* y, const uint8_t* qs, const u
     if (!p.fault) return cudaErrorInvalidSymbol;
     p.slot_bytes = round_up((uint32_t)(R * nblk * 18), 128u);
     p.xs_off = 512;
-    p.fac_off = p.xs_off + (PURE ? 0u : (uint32_t)UPL * 4096u);
+    p.fac_off = p.xs_off + (PURE ? 0u : (uint32_t)UPL * 8u * kXRow * 16u);
     p.slots_off = round_up(p.fac_off + (PURE ? 0u : (uint32_t)UPL * 128u), 128u);
     const uint32_t smem = p.slots_off + (uint32_t)(W * D) * p.slot_bytes;
     if (smem > (uint32_t)di.max_smem_optin) return cudaErrorNotSupported;

@@ -634,11 +634,13 @@ def measure_per_call(suite, inputs, table, stream, peak, fma_rate=None):
         out.append(_entry(table[j][0], table[j][1], us, spread, k, peak, fmas=fmas[j], fma_rate=fma_rate, **extra))
 
     cp, k = cold_copies(w["c1"], table[0][1])
-    one(0, [lambda c=c: q4.q4_gemv(suite.y1, c[0], c[1], suite.x1, stream=stream) for c in cp], k)
+    one(0, [lambda c=c: q4.q4_gemv(suite.y1, c[0], c[1], suite.x1, stream=stream) for c in cp], k,
+        pure=[lambda c=c: q4.q4_pure_read(suite.y1, c[0], c[1], stream=stream) for c in cp])
     del cp
     cp, k = cold_copies((w["c2"],), table[1][1])
     one(1, [lambda c=c: q4.fused_rmsnorm_q4k_gemv(suite.y2, c[0], suite.x2, suite.g2, c2eps, stream=stream)
-            for c in cp], k)
+            for c in cp], k,
+        pure=[lambda c=c: q4.q4k_pure_read(suite.y2, c[0], stream=stream) for c in cp])
     del cp
     cp, k = cold_copies(w["c3"], table[2][1])
     one(2, [lambda c=c: q4.fused_gateup_q4k_gemv(suite.y3g, suite.y3u, c[0], c[1], suite.x3, suite.g3, c3eps,

@@ -787,7 +787,11 @@ def cpu_baseline(inputs):
         oracle_step(o, inputs, 1.0 / 64, pool, parts)
         t_full = (time.perf_counter() - t0) * 64
         frac = min(1.0, 10.0 / t_full)  # aim at about 10 s of host work: a row sample, or whole passes
-        passes = max(1, int(round(10.0 / t_full))) if frac == 1.0 else 1
+        passes = 1
+        if frac == 1.0:  # time one whole pass, then repeat it to about 10 s
+            t0 = time.perf_counter()
+            oracle_step(o, inputs, 1.0, pool, parts)
+            passes = max(1, int(round(10.0 / (time.perf_counter() - t0))))
         t0 = time.perf_counter()
         done = sum(oracle_step(o, inputs, frac, pool, parts) for _ in range(passes))
         dt = time.perf_counter() - t0

@@ -76,6 +76,13 @@ __host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (
 // routings with 1, 2 and 4 slots per expert). The pure-read instrument costs the same for every C.
 __device__ __forceinline__ long long job_cost(int C, bool pure, int a, int b) { return pure ? 1 : a + (long long)b * C; }
 
+// floor(a / b) for 0 <= a and 0 < b, as a 32-bit division whenever both fit (a 64-bit integer division is a long
+// emulated sequence, and every warp needs a few at its start).
+__device__ __forceinline__ long long floor_div(long long a, long long b) {
+    if (a < 0x80000000LL && b < 0x80000000LL) return (long long)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 __host__ __device__ constexpr uint32_t moe_slot_bytes(int R, int UPL) {
     return (uint32_t)(((R * 32 * UPL * 18) + 127) / 128 * 128);
 }
@@ -127,6 +134,26 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     grid_dependency_wait();
     grid_launch_dependents();
 
+    // The inputs' first staging batch does not depend on the routing: its loads are issued now and land while the
+    // routing runs. Each thread takes up to kBatch block quarters (four lanes per 32-element block).
+    constexpr int kBatch = 8;
+    const int nb_all = p.T * p.nblk;
+    const int nthr = (nb_all * 4 + 31) & ~31;  // whole warps, so the group shuffles always see 32 lanes
+    float4 xa[PURE ? 1 : kBatch], xb[PURE ? 1 : kBatch];
+    auto load_batch = [&](int base) {
+        if constexpr (!PURE) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int blk = (base + j * kThreads) >> 2;
+                const bool in = blk < nb_all;
+                const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * (lane & 3);
+                xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    load_batch((int)threadIdx.x);
+
     // ---- routing -------------------------------------------------------------------------------------
     for (int i = threadIdx.x; i < TK; i += kThreads) {
         slot_ids[i] = __ldg(p.ids + i);
@@ -137,11 +164,14 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         const int e = slot_ids[i];
         int first = -1, rk = 0;
         if (e >= 0 && e < p.E) {
-            for (int j = 0; j < i; ++j) {
-                if (slot_ids[j] == e) {
-                    if (first < 0) first = j;
-                    ++rk;
-                }
+            // the earlier slots four at a time (the table starts 16-byte aligned and has ms >= TK entries)
+            const int4* const s4 = reinterpret_cast<const int4*>(slot_ids);
+            for (int j = 0; j < i; j += 4) {
+                const int4 v = s4[j >> 2];
+                const bool m0 = v.x == e, m1 = v.y == e && j + 1 < i, m2 = v.z == e && j + 2 < i,
+                           m3 = v.w == e && j + 3 < i;
+                if (first < 0) first = m0 ? j : m1 ? j + 1 : m2 ? j + 2 : m3 ? j + 3 : -1;
+                rk += (int)m0 + (int)m1 + (int)m2 + (int)m3;
             }
             if (first < 0) first = i;
         }
@@ -293,10 +323,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             if (gcum[mid] <= c) lo = mid;
             else hi = mid - 1;
         }
-        return lo * NP * rgs + (int)((c - gcum[lo]) / job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
+        return lo * NP * rgs + (int)floor_div(c - gcum[lo], job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
     };
-    const int j0 = p.deal ? gw : job_at(total_cost * gw / Wtot);
-    const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : job_at(total_cost * (gw + 1) / Wtot);
+    const int j0 = p.deal ? gw : job_at(floor_div(total_cost * gw, Wtot));
+    const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : job_at(floor_div(total_cost * (gw + 1), Wtot));
     const int jstep = p.deal ? Wtot : 1;  // job stride of this warp
     const uint64_t pol = policy_evict_first();
 
@@ -393,37 +423,40 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         // Stage the T tokens: four lanes per 32-element block, lane t of the group holding quads 2t and 2t+1
         // (block sum and largest magnitude by two group shuffles); the loop covers whole warps so the
         // shuffles always see 32 lanes.
-        const int nb_all = p.T * U;
         const int t4 = lane & 3;
-        const int nthr = (nb_all * 4 + 31) & ~31;
-        for (int thr = threadIdx.x; thr < nthr; thr += kThreads) {
-            const int blk = thr >> 2;
-            const bool in = blk < nb_all;
-            const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * t4;
-            const float4 xa = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 xb = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const Stage4 st = stage_block4(xa, xb, t4 >> 1);
-            if (in) {
-                const int v = blk / U;
-                const int u = blk - v * U;
-                // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise [token][quad][block]
-                // (16 bytes each): the lanes of a warp read consecutive 16-byte pieces either way
-                const int grp32 = u >> 5, ul = u & 31;
-                const int q0 = 2 * t4;
-                const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
-                                                       : ((v * 8 + q0) * U + u) * 16);
-                const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
-                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
-                             "f"(st.a.z), "f"(st.a.w)
-                             : "memory");
-                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x), "f"(st.b.y),
-                             "f"(st.b.z), "f"(st.b.w)
-                             : "memory");
-                if (t4 == 0)
-                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
-                                                                                                : v * U + u) * 8)),
-                                 "f"(block_factor(st.e)), "f"(0.0f)
+        // Each thread issues the loads of up to kBatch of its block quarters before using any of them, so staging
+        // costs one round trip to the L2 per kBatch quarters rather than one per quarter (the first batch's loads
+        // were issued before the routing).
+        for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
+            if (base != (int)threadIdx.x) load_batch(base);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int thr = base + j * kThreads;
+                if (thr >= nthr) break;  // warp-uniform: the group shuffles always see 32 lanes
+                const int blk = thr >> 2;
+                const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
+                if (blk < nb_all) {
+                    const int v = blk / U;
+                    const int u = blk - v * U;
+                    // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise
+                    // [token][quad][block] (16 bytes each): the lanes of a warp read consecutive 16-byte pieces
+                    const int grp32 = u >> 5, ul = u & 31;
+                    const int q0 = 2 * t4;
+                    const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
+                                                           : ((v * 8 + q0) * U + u) * 16);
+                    const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
+                                 "f"(st.a.z), "f"(st.a.w)
                                  : "memory");
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x),
+                                 "f"(st.b.y), "f"(st.b.z), "f"(st.b.w)
+                                 : "memory");
+                    if (t4 == 0)
+                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
+                                                                                                : v * U + u) * 8)),
+                                     "f"(block_factor(st.e)), "f"(0.0f)
+                                     : "memory");
+                }
             }
         }
         __syncthreads();

@@ -161,10 +161,13 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
         const int nb_all = V * p.nblk;
         const int t4 = lane & 3;
         const int nthr = ((nb_all * 4 + 31) & ~31);
-        for (int base = threadIdx.x; base < nthr; base += kThreads * (kStageU / 2)) {
-            float4 xa[kStageU / 2], xb[kStageU / 2];
+        // each thread issues the loads of kBatch block quarters before using any (batches of 8 for the wider
+        // inputs, whose staging would otherwise take one L2 round trip per 4 quarters)
+        constexpr int kBatch = V >= 2 ? 8 : kStageU / 2;
+        for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
+            float4 xa[kBatch], xb[kBatch];
 #pragma unroll
-            for (int j = 0; j < kStageU / 2; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const int blk = (base + j * kThreads) >> 2;
                 const bool in = blk < nb_all;
                 const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * t4;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int j = 0; j < kStageU / 2; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const int thr = base + j * kThreads;
                 if (thr >= nthr) break;  // warp-uniform
                 const int blk = thr >> 2;

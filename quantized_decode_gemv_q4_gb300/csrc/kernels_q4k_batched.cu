@@ -92,16 +92,31 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
     grid_dependency_wait();
     grid_launch_dependents();
 
-    // Stage the V vectors: four lanes per sub-block (whole warps: V*K/32*4 is a multiple of 32).
+    // Stage the V vectors: four lanes per sub-block (whole warps: V*K/32*4 is a multiple of 32). Each thread issues
+    // the loads of up to kBatch of its sub-block quarters before using any of them (one L2 round trip per batch).
     {
         const int t4 = lane & 3;
-        for (int thr = threadIdx.x; thr < V * nsub * 4; thr += kThreads) {
+        const int nthr = V * nsub * 4;
+        constexpr int kBatch = 8;
+        for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
+        float4 xa[kBatch], xb[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int thr = base + j * kThreads;
+            const bool in = thr < nthr;
+            const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)(in ? thr >> 2 : 0) * 8 + 2 * t4;
+            xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int jb = 0; jb < kBatch; ++jb) {
+            const int thr = base + jb * kThreads;
+            if (thr >= nthr) break;  // warp-uniform
             const int jsv = thr >> 2;  // v * nsub + js
             const int v = jsv / nsub;
             const int js = jsv - v * nsub;
-            const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)jsv * 8 + 2 * t4;
             const int k = js & 1;
-            const Stage4 st = stage_block4(__ldg(src), __ldg(src + 1), k);
+            const Stage4 st = stage_block4(xa[jb], xb[jb], k);
             const uint32_t u = (uint32_t)(js & ~1) + (uint32_t)(t4 >> 1);
             const uint32_t q0 = (uint32_t)(4 * k + ((2 * t4) & 3));
             const uint32_t a0 = xs + xs_index((uint32_t)v, q0, u, U) * 4u;
@@ -117,6 +132,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(ua), "f"(block_factor(st.e)) : "memory");
                 asm volatile("st.shared.f32 [%0], %1;" ::"r"(ua + 16u), "f"(block_factor(st.e)) : "memory");
             }
+        }
         }
         __syncthreads();
         // S of each unit's two halves: the unit chain on codes of 1 (low pairs over quads 0..3, high over 4..7)

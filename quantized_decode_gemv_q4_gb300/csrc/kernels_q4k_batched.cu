@@ -338,7 +338,8 @@ cudaError_t run_batched(const DeviceInfo& di, float* Y, const uint8_t* w, const 
 
 }  // namespace
 
-// Variant per batch width: 16 warps x 2 rows for one or two vectors, 8 warps x 2 rows above.
+// Variant per batch width: 16 warps x 2 rows for one or two vectors, 8 warps x 2 rows for three, 8 x 4 for four
+// and 8 x 3 for five to eight (each staged quad serves more rows; four rows at eight vectors would spill).
 cudaError_t launch_q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, int V, int N, int K, cudaStream_t s) {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
@@ -350,11 +351,11 @@ cudaError_t launch_q4k_gemv_batched(float* Y, const uint8_t* w, const float* X, 
             return e == cudaErrorNotSupported ? run_batched<1, 2, 16>(di, Y, w, X, N, K, s) : e;
         case 2: return run_batched<2, 2, 16>(di, Y, w, X, N, K, s);
         case 3: return run_batched<3, 2, 8>(di, Y, w, X, N, K, s);
-        case 4: return run_batched<4, 2, 8>(di, Y, w, X, N, K, s);
-        case 5: return run_batched<5, 2, 8>(di, Y, w, X, N, K, s);
-        case 6: return run_batched<6, 2, 8>(di, Y, w, X, N, K, s);
-        case 7: return run_batched<7, 2, 8>(di, Y, w, X, N, K, s);
-        case 8: return run_batched<8, 2, 8>(di, Y, w, X, N, K, s);
+        case 4: return run_batched<4, 4, 8>(di, Y, w, X, N, K, s);
+        case 5: return run_batched<5, 3, 8>(di, Y, w, X, N, K, s);
+        case 6: return run_batched<6, 3, 8>(di, Y, w, X, N, K, s);
+        case 7: return run_batched<7, 3, 8>(di, Y, w, X, N, K, s);
+        case 8: return run_batched<8, 3, 8>(di, Y, w, X, N, K, s);
         default: return cudaErrorInvalidValue;
     }
 }

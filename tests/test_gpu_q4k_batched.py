@@ -19,7 +19,7 @@ def oracle_rows(oracle_lib, w, X):
 
 
 @pytest.mark.parametrize("N,K,M", [(3584, 3584, 1), (3584, 3584, 8), (18944, 3584, 4), (300, 256, 3), (1001, 4096, 8),
-                                   (17, 512, 2), (5000, 1280, 5)])
+                                   (17, 512, 2), (5000, 1280, 5), (777, 2048, 6), (1500, 3584, 7)])
 def test_q4k_batched_matches_oracle(N, K, M, oracle_lib):
     rng = np.random.default_rng(N + K + M)
     w = synth.q4k_weights(rng, N, K)

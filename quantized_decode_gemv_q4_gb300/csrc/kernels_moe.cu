@@ -68,8 +68,9 @@ struct MoEParams {
 // Routing tables in shared memory (route_off), each of ms = T*topk rounded up to 32 entries: slot_ids, rank,
 // owner, ucount, uoffset (ms+1), list, group_ux, group_first, group_cnt, scalars[4] (number of distinct experts,
 // number of groups), then the cumulative job cost gcum[ms+1] (64-bit), the job order of the groups gorder
-// (groups sorted by slot count), the token of each list entry ltok and the expert id of each group group_eid.
-__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 3 * ms; }
+// (groups sorted by slot count), the token of each list entry ltok, the expert id of each group group_eid and the
+// first job of each of the CTA's warps and of the next CTA (17 entries).
+__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 3 * ms + 17; }
 
 // Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
 // (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
@@ -128,143 +129,12 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     int* gorder = route + 9 * ms + 8 + 2 * (ms + 1) + 2;
     int* ltok = gorder + ms;  // token of each list entry (slot / topk), so stages divide nothing
     int* group_eid = ltok + ms;  // expert id of each group
+    int* jr = group_eid + ms;    // job ranges of the CTA's warps: warp w takes [jr[w], jr[w + 1])
 
-    // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
-    // in the stream (it may have written ids, x or the outputs) before anything else.
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    // The inputs' first staging batch does not depend on the routing: its loads are issued now and land while the
-    // routing runs. Each thread takes up to kBatch block quarters (four lanes per 32-element block).
-    constexpr int kBatch = 8;
-    const int nb_all = p.T * p.nblk;
-    const int nthr = (nb_all * 4 + 31) & ~31;  // whole warps, so the group shuffles always see 32 lanes
-    float4 xa[PURE ? 1 : kBatch], xb[PURE ? 1 : kBatch];
-    auto load_batch = [&](int base) {
-        if constexpr (!PURE) {
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int blk = (base + j * kThreads) >> 2;
-                const bool in = blk < nb_all;
-                const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)blk * 8 + 2 * (lane & 3);
-                xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-                xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-    };
-    load_batch((int)threadIdx.x);
-
-    // ---- routing -------------------------------------------------------------------------------------
-    for (int i = threadIdx.x; i < TK; i += kThreads) {
-        slot_ids[i] = __ldg(p.ids + i);
-        ucount[i] = 0;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < TK; i += kThreads) {
-        const int e = slot_ids[i];
-        int first = -1, rk = 0;
-        if (e >= 0 && e < p.E) {
-            // the earlier slots four at a time (the table starts 16-byte aligned and has ms >= TK entries)
-            const int4* const s4 = reinterpret_cast<const int4*>(slot_ids);
-            for (int j = 0; j < i; j += 4) {
-                const int4 v = s4[j >> 2];
-                const bool m0 = v.x == e, m1 = v.y == e && j + 1 < i, m2 = v.z == e && j + 2 < i,
-                           m3 = v.w == e && j + 3 < i;
-                if (first < 0) first = m0 ? j : m1 ? j + 1 : m2 ? j + 2 : m3 ? j + 3 : -1;
-                rk += (int)m0 + (int)m1 + (int)m2 + (int)m3;
-            }
-            if (first < 0) first = i;
-        }
-        owner[i] = first;  // -1: invalid id
-        rank[i] = rk;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // number the distinct experts (first slots) in slot order
-        int base = 0;
-        for (int c0 = 0; c0 < TK; c0 += 32) {
-            const int i = c0 + lane;
-            const bool first = i < TK && owner[i] == i;
-            const unsigned m = __ballot_sync(0xffffffffu, first);
-            if (first) list[i] = base + __popc(m & ((1u << lane) - 1u));  // temporary: ux of first slot i
-            base += __popc(m);
-        }
-        if (lane == 0) scalars[0] = base;
-    }
-    __syncthreads();
-    const int nux = scalars[0];
-    for (int i = threadIdx.x; i < TK; i += kThreads) {
-        const int f = owner[i];
-        if (f >= 0) {
-            const int ux = list[f];
-            owner[i] = ux;  // from here on: distinct-expert index of slot i
-            atomicAdd(&ucount[ux], 1);
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // exclusive prefix sums of slot counts and of groups per distinct expert
-        int base = 0, gbase = 0;
-        for (int c0 = 0; c0 < nux; c0 += 32) {
-            const int u = c0 + lane;
-            const int cnt = u < nux ? ucount[u] : 0;
-            const int ng = (cnt + kMaxC - 1) / kMaxC;
-            int incl = cnt, gincl = ng;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int a = __shfl_up_sync(0xffffffffu, incl, off);
-                const int b = __shfl_up_sync(0xffffffffu, gincl, off);
-                if (lane >= off) {
-                    incl += a;
-                    gincl += b;
-                }
-            }
-            if (u < nux) {
-                uoffset[u] = base + incl - cnt;
-                const int g0 = gbase + gincl - ng;
-                for (int gi = 0; gi < ng; ++gi) {
-                    group_ux[g0 + gi] = u;
-                    group_first[g0 + gi] = uoffset[u] + gi * kMaxC;
-                    group_cnt[g0 + gi] = min(kMaxC, cnt - gi * kMaxC);
-                }
-            }
-            base += __shfl_sync(0xffffffffu, incl, 31);
-            gbase += __shfl_sync(0xffffffffu, gincl, 31);
-        }
-        if (lane == 0) scalars[1] = gbase;
-    }
-    __syncthreads();
-    const int ngroups = scalars[1];
-    for (int i = threadIdx.x; i < TK; i += kThreads) {
-        const int ux = owner[i];
-        if (ux >= 0) {
-            list[uoffset[ux] + rank[i]] = i;
-            ltok[uoffset[ux] + rank[i]] = i / p.topk;
-        }
-    }
-    __syncthreads();
-    // group -> expert id
-    for (int gi = threadIdx.x; gi < ngroups; gi += kThreads) group_eid[gi] = slot_ids[list[uoffset[group_ux[gi]]]];
-    // invalid slots: NaN outputs and a status bit (CTA 0 only)
-    if (blockIdx.x == 0) {
-        for (int i = 0; i < TK; ++i) {
-            if (owner[i] >= 0) continue;
-            for (int r = threadIdx.x; r < p.N; r += kThreads) {
-                p.yg[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);
-                if constexpr (!SWIGLU) p.yu[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);  // no y_up
-            }
-            if (threadIdx.x == 0) {
-                if (p.status) atomicOr(reinterpret_cast<unsigned*>(p.status), (unsigned)kFaultBadExpert);
-                atomicOr(p.fault, (unsigned)kFaultBadExpert);
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- jobs -------------------------------------------------------------------------------------------
     const uint32_t s_base = smem_addr(smem);
     const uint32_t xs = s_base + p.xs_off;
     const uint32_t aux = s_base + p.aux_off;
+    const int U = p.nblk;
     const uint32_t ring = s_base + p.slots_off + (uint32_t)warp * (uint32_t)(D * SLOT);
     const uint32_t bars = s_base + p.bar_off + (uint32_t)(warp * D) * 8u;  // one mbarrier per slot (bulk mode)
     if (p.bulk) {
@@ -275,19 +145,79 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         }
         __syncwarp();
     }
-    const int U = p.nblk;
     const int rgs = (p.N + R - 1) / R;
-    const int jobs = ngroups * NP * rgs;
     // Groups run in order of slot count. Round-robin dealing (p.deal = 1): warp gw (numbered across CTAs
     // first) takes jobs gw, gw + Wtot, ..., so at any moment the grid sweeps neighbouring rows of one expert
     // matrix and the warps of an SM run the same compiled stage body. Range dealing (p.deal = 0): warps
     // numbered CTA by CTA own contiguous job ranges of equal estimated cost.
     const int gw = p.deal ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * W + warp;
     const int Wtot = (int)gridDim.x * W;
+
+    // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
+    // in the stream (it may have written ids, x or the outputs) before anything else.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // Staging of the T inputs by threads t0 .. t0 + cnt - 1 (whole warps): four lanes per 32-element block, lane
+    // t of the group holding quads 2t and 2t+1 (block sum and largest magnitude by two group shuffles). Each
+    // thread issues the loads of up to kBatch of its block quarters before using any, so staging costs one round
+    // trip to the L2 per kBatch quarters.
+    constexpr int kBatch = 12;
+    const int nb_all = p.T * U;
+    const int nthr = (nb_all * 4 + 31) & ~31;  // whole warps, so the group shuffles always see 32 lanes
+    auto stage_inputs = [&](int t0, int cnt) {
+        if constexpr (!PURE) {
+            const int me = (int)threadIdx.x - t0;
+            const int t4 = lane & 3;
+            for (int base = me; base < nthr; base += cnt * kBatch) {
+                float4 xa[kBatch], xb[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int blk = (base + j * cnt) >> 2;
+                    const bool in = blk < nb_all;
+                    const float4* src = reinterpret_cast<const float4*>(p.x) + (size_t)(in ? blk : 0) * 8 + 2 * t4;
+                    xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int thr = base + j * cnt;
+                    if (thr >= nthr) break;  // warp-uniform
+                    const int blk = thr >> 2;
+                    const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
+                    if (blk < nb_all) {
+                        const int v = blk / U;
+                        const int u = blk - v * U;
+                        // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise
+                        // [token][quad][block] (16 bytes each): the lanes of a warp read consecutive 16-byte pieces
+                        const int grp32 = u >> 5, ul = u & 31;
+                        const int q0 = 2 * t4;
+                        const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
+                                                               : ((v * 8 + q0) * U + u) * 16);
+                        const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
+                                     "f"(st.a.z), "f"(st.a.w)
+                                     : "memory");
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x),
+                                     "f"(st.b.y), "f"(st.b.z), "f"(st.b.w)
+                                     : "memory");
+                        if (t4 == 0)
+                            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
+                                                                                                    : v * U + u) * 8)),
+                                         "f"(block_factor(st.e)), "f"(0.0f)
+                                         : "memory");
+                    }
+                }
+            }
+        }
+    };
+
     // Job order of the groups (stable by slot count), then the cumulative cost in that order (each group has
     // 2 * rgs jobs of cost job_cost(cnt)), then this warp's share of the total cost as a contiguous job range
     // [j0, j1): groups with more routed slots spread over more warps.
-    if (warp == 0) {
+    auto order_and_ranges = [&]() {
+        const int ngroups = scalars[1];
+        const int jobs = ngroups * NP * rgs;
         int base = 0;
         for (int c = 1; c <= kMaxC; ++c) {
             for (int c0 = 0; c0 < ngroups; c0 += 32) {
@@ -312,21 +242,220 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             cb += __shfl_sync(0xffffffffu, v, 31);
         }
         if (lane == 0) gcum[0] = 0;
-    }
-    __syncthreads();
-    const long long total_cost = gcum[ngroups];
-    auto job_at = [&](long long c) {  // the job that holds cost offset c
-        if (c >= total_cost) return jobs;
-        int lo = 0, hi = ngroups - 1;  // largest g with gcum[g] <= c
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (gcum[mid] <= c) lo = mid;
-            else hi = mid - 1;
+        __syncwarp();
+        // the first job of each of this CTA's warps and of the next CTA's first warp (range dealing)
+        if (!p.deal && lane <= W) {
+            const long long c = floor_div(cb * ((int)blockIdx.x * W + lane), Wtot);
+            int j = jobs;
+            if (c < cb) {
+                int lo = 0, hi = ngroups - 1;  // largest g with gcum[g] <= c
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (gcum[mid] <= c) lo = mid;
+                    else hi = mid - 1;
+                }
+                j = lo * NP * rgs + (int)floor_div(c - gcum[lo], job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
+            }
+            jr[lane] = j;
         }
-        return lo * NP * rgs + (int)floor_div(c - gcum[lo], job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
     };
-    const int j0 = p.deal ? gw : job_at(floor_div(total_cost * gw, Wtot));
-    const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : job_at(floor_div(total_cost * (gw + 1), Wtot));
+
+    // ---- routing, with the inputs staged beside it --------------------------------------------------
+    if (TK <= 64) {
+        // Warp 0 routes alone, two slots per lane (slots lane and lane + 32), while the other warps stage the
+        // inputs. Equal experts within a half are found by match, across the halves by 32 shuffles; an invalid or
+        // absent slot gets a key no other slot has. The tables come out as the general path's.
+        if (warp == 0) {
+            const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
+            const int i0 = lane, i1 = lane + 32;
+            const int e0 = i0 < TK ? __ldg(p.ids + i0) : -1;
+            const int e1 = i1 < TK ? __ldg(p.ids + i1) : -1;
+            const bool v0 = i0 < TK && e0 >= 0 && e0 < p.E, v1 = i1 < TK && e1 >= 0 && e1 < p.E;
+            const int k0 = v0 ? e0 : -1 - i0, k1 = v1 ? e1 : -1 - i1;
+            const unsigned m0 = __match_any_sync(full, k0), m1 = __match_any_sync(full, k1);
+            int c10 = 0, f10 = -1, c01 = 0;  // slot i1's equals among slots 0..31 (count, first); slot i0's among 32..63
+            for (int k = 0; k < 32; ++k) {
+                const int a = __shfl_sync(full, k0, k), b = __shfl_sync(full, k1, k);
+                if (a == k1) {
+                    if (f10 < 0) f10 = k;
+                    ++c10;
+                }
+                if (b == k0) ++c01;
+            }
+            const int rank0 = __popc(m0 & lt), first0 = __ffs(m0) - 1;
+            const int rank1 = c10 + __popc(m1 & lt), first1 = f10 >= 0 ? f10 : 32 + __ffs(m1) - 1;
+            const bool isf0 = v0 && first0 == i0, isf1 = v1 && first1 == i1;
+            // distinct experts numbered by first appearance (slots 0..31, then 32..63)
+            const unsigned b0 = __ballot_sync(full, isf0), b1 = __ballot_sync(full, isf1);
+            const int nux0 = __popc(b0);
+            const int uxf0 = __popc(b0 & lt), uxf1 = nux0 + __popc(b1 & lt);  // on first slots
+            // each expert's slot count and group count on its first slot, then exclusive prefix sums in that order
+            const int cnt0 = isf0 ? __popc(m0) + c01 : 0, cnt1 = isf1 ? __popc(m1) : 0;
+            const int ng0 = (cnt0 + kMaxC - 1) / kMaxC, ng1 = (cnt1 + kMaxC - 1) / kMaxC;
+            int ic0 = cnt0, ig0 = ng0, ic1 = cnt1, ig1 = ng1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int a = __shfl_up_sync(full, ic0, off), b = __shfl_up_sync(full, ig0, off);
+                const int c = __shfl_up_sync(full, ic1, off), d = __shfl_up_sync(full, ig1, off);
+                if (lane >= off) {
+                    ic0 += a;
+                    ig0 += b;
+                    ic1 += c;
+                    ig1 += d;
+                }
+            }
+            const int tc0 = __shfl_sync(full, ic0, 31), tg0 = __shfl_sync(full, ig0, 31);
+            const int ngroups_f = tg0 + __shfl_sync(full, ig1, 31);
+            const int uoff0 = ic0 - cnt0, goff0 = ig0 - ng0;
+            const int uoff1 = tc0 + ic1 - cnt1, goff1 = tg0 + ig1 - ng1;
+            if (isf0)
+                for (int gi = 0; gi < ng0; ++gi) {
+                    group_ux[goff0 + gi] = uxf0;
+                    group_first[goff0 + gi] = uoff0 + gi * kMaxC;
+                    group_cnt[goff0 + gi] = min(kMaxC, cnt0 - gi * kMaxC);
+                    group_eid[goff0 + gi] = e0;
+                }
+            if (isf1)
+                for (int gi = 0; gi < ng1; ++gi) {
+                    group_ux[goff1 + gi] = uxf1;
+                    group_first[goff1 + gi] = uoff1 + gi * kMaxC;
+                    group_cnt[goff1 + gi] = min(kMaxC, cnt1 - gi * kMaxC);
+                    group_eid[goff1 + gi] = e1;
+                }
+            // each slot's expert index and list position, from its first slot's lane
+            const int ux0 = __shfl_sync(full, uxf0, first0 & 31);
+            const int uo0 = __shfl_sync(full, uoff0, first0 & 31);
+            const int ux1a = __shfl_sync(full, uxf0, first1 & 31), ux1b = __shfl_sync(full, uxf1, first1 & 31);
+            const int uo1a = __shfl_sync(full, uoff0, first1 & 31), uo1b = __shfl_sync(full, uoff1, first1 & 31);
+            const int ux1 = first1 < 32 ? ux1a : ux1b, uo1 = first1 < 32 ? uo1a : uo1b;
+            if (i0 < TK) {
+                slot_ids[i0] = e0;
+                owner[i0] = v0 ? ux0 : -1;
+                if (v0) {
+                    list[uo0 + rank0] = i0;
+                    ltok[uo0 + rank0] = i0 / p.topk;
+                }
+            }
+            if (i1 < TK) {
+                slot_ids[i1] = e1;
+                owner[i1] = v1 ? ux1 : -1;
+                if (v1) {
+                    list[uo1 + rank1] = i1;
+                    ltok[uo1 + rank1] = i1 / p.topk;
+                }
+            }
+            if (lane == 0) {
+                scalars[0] = nux0 + __popc(b1);
+                scalars[1] = ngroups_f;
+            }
+            __syncwarp();
+            order_and_ranges();
+        } else {
+            stage_inputs(32, kThreads - 32);
+        }
+        __syncthreads();
+    } else {
+        for (int i = threadIdx.x; i < TK; i += kThreads) {
+            slot_ids[i] = __ldg(p.ids + i);
+            ucount[i] = 0;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < TK; i += kThreads) {
+            const int e = slot_ids[i];
+            int first = -1, rk = 0;
+            if (e >= 0 && e < p.E) {
+                // the earlier slots four at a time (the table starts 16-byte aligned and has ms >= TK entries)
+                const int4* const s4 = reinterpret_cast<const int4*>(slot_ids);
+                for (int j = 0; j < i; j += 4) {
+                    const int4 v = s4[j >> 2];
+                    const bool m0 = v.x == e, m1 = v.y == e && j + 1 < i, m2 = v.z == e && j + 2 < i,
+                               m3 = v.w == e && j + 3 < i;
+                    if (first < 0) first = m0 ? j : m1 ? j + 1 : m2 ? j + 2 : m3 ? j + 3 : -1;
+                    rk += (int)m0 + (int)m1 + (int)m2 + (int)m3;
+                }
+                if (first < 0) first = i;
+            }
+            owner[i] = first;  // -1: invalid id
+            rank[i] = rk;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // number the distinct experts (first slots) in slot order
+            int base = 0;
+            for (int c0 = 0; c0 < TK; c0 += 32) {
+                const int i = c0 + lane;
+                const bool first = i < TK && owner[i] == i;
+                const unsigned m = __ballot_sync(0xffffffffu, first);
+                if (first) list[i] = base + __popc(m & ((1u << lane) - 1u));  // temporary: ux of first slot i
+                base += __popc(m);
+            }
+            if (lane == 0) scalars[0] = base;
+        }
+        __syncthreads();
+        const int nux = scalars[0];
+        for (int i = threadIdx.x; i < TK; i += kThreads) {
+            const int f = owner[i];
+            if (f >= 0) {
+                const int ux = list[f];
+                owner[i] = ux;  // from here on: distinct-expert index of slot i
+                atomicAdd(&ucount[ux], 1);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive prefix sums of slot counts and of groups per distinct expert
+            int base = 0, gbase = 0;
+            for (int c0 = 0; c0 < nux; c0 += 32) {
+                const int u = c0 + lane;
+                const int cnt = u < nux ? ucount[u] : 0;
+                const int ng = (cnt + kMaxC - 1) / kMaxC;
+                int incl = cnt, gincl = ng;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int a = __shfl_up_sync(0xffffffffu, incl, off);
+                    const int b = __shfl_up_sync(0xffffffffu, gincl, off);
+                    if (lane >= off) {
+                        incl += a;
+                        gincl += b;
+                    }
+                }
+                if (u < nux) {
+                    uoffset[u] = base + incl - cnt;
+                    const int g0 = gbase + gincl - ng;
+                    for (int gi = 0; gi < ng; ++gi) {
+                        group_ux[g0 + gi] = u;
+                        group_first[g0 + gi] = uoffset[u] + gi * kMaxC;
+                        group_cnt[g0 + gi] = min(kMaxC, cnt - gi * kMaxC);
+                    }
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+                gbase += __shfl_sync(0xffffffffu, gincl, 31);
+            }
+            if (lane == 0) scalars[1] = gbase;
+        }
+        __syncthreads();
+        const int ngr = scalars[1];
+        for (int i = threadIdx.x; i < TK; i += kThreads) {
+            const int ux = owner[i];
+            if (ux >= 0) {
+                list[uoffset[ux] + rank[i]] = i;
+                ltok[uoffset[ux] + rank[i]] = i / p.topk;
+            }
+        }
+        __syncthreads();
+        // group -> expert id
+        for (int gi = threadIdx.x; gi < ngr; gi += kThreads) group_eid[gi] = slot_ids[list[uoffset[group_ux[gi]]]];
+        __syncthreads();
+        if (warp == 0) order_and_ranges();
+        else stage_inputs(32, kThreads - 32);
+        __syncthreads();
+    }
+    const int ngroups = scalars[1];
+
+    // ---- jobs -------------------------------------------------------------------------------------------
+    const int jobs = ngroups * NP * rgs;
+    const int j0 = p.deal ? gw : jr[warp];
+    const int j1 = p.deal ? (gw < jobs ? gw + ((jobs - 1 - gw) / Wtot + 1) : gw) : jr[warp + 1];
     const int jstep = p.deal ? Wtot : 1;  // job stride of this warp
     const uint64_t pol = policy_evict_first();
 
@@ -419,48 +548,9 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
 #pragma unroll
     for (int k = 0; k < D - 1; ++k) issue();
 
+    // With the first copies in flight: each block's -8 offset term (the unit chain on codes of 8 over its staged
+    // quads) and, in CTA 0, the invalid slots' NaN rows and status bit.
     if constexpr (!PURE) {
-        // Stage the T tokens: four lanes per 32-element block, lane t of the group holding quads 2t and 2t+1
-        // (block sum and largest magnitude by two group shuffles); the loop covers whole warps so the
-        // shuffles always see 32 lanes.
-        const int t4 = lane & 3;
-        // Each thread issues the loads of up to kBatch of its block quarters before using any of them, so staging
-        // costs one round trip to the L2 per kBatch quarters rather than one per quarter (the first batch's loads
-        // were issued before the routing).
-        for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
-            if (base != (int)threadIdx.x) load_batch(base);
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int thr = base + j * kThreads;
-                if (thr >= nthr) break;  // warp-uniform: the group shuffles always see 32 lanes
-                const int blk = thr >> 2;
-                const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
-                if (blk < nb_all) {
-                    const int v = blk / U;
-                    const int u = blk - v * U;
-                    // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise
-                    // [token][quad][block] (16 bytes each): the lanes of a warp read consecutive 16-byte pieces
-                    const int grp32 = u >> 5, ul = u & 31;
-                    const int q0 = 2 * t4;
-                    const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
-                                                           : ((v * 8 + q0) * U + u) * 16);
-                    const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
-                                 "f"(st.a.z), "f"(st.a.w)
-                                 : "memory");
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x),
-                                 "f"(st.b.y), "f"(st.b.z), "f"(st.b.w)
-                                 : "memory");
-                    if (t4 == 0)
-                        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
-                                                                                                : v * U + u) * 8)),
-                                     "f"(block_factor(st.e)), "f"(0.0f)
-                                     : "memory");
-                }
-            }
-        }
-        __syncthreads();
-        // each block's -8 offset term: the unit chain on codes of 8 over its staged quads
         for (int b = threadIdx.x; b < nb_all; b += kThreads) {
             const int v = b / U;
             const int u = b - v * U;
@@ -473,6 +563,19 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
             const uint32_t a = aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul : v * U + u) * 8);
             const float bias = q4_block_bias(xq, lds32f(a));
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 4u), "f"(bias) : "memory");
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (int i = 0; i < TK; ++i) {
+            if (owner[i] >= 0) continue;
+            for (int r = threadIdx.x; r < p.N; r += kThreads) {
+                p.yg[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);
+                if constexpr (!SWIGLU) p.yu[(size_t)i * p.N + r] = __int_as_float(0x7fc00000);  // no y_up
+            }
+            if (threadIdx.x == 0) {
+                if (p.status) atomicOr(reinterpret_cast<unsigned*>(p.status), (unsigned)kFaultBadExpert);
+                atomicOr(p.fault, (unsigned)kFaultBadExpert);
+            }
         }
     }
     __syncthreads();

@@ -283,41 +283,10 @@ __host__ __device__ __forceinline__ uint32_t aux_bytes(uint32_t V, uint32_t U) {
 //
 // For V input vectors of length K the staged copy is float[V][8][U][4] with U = K/32 sixteen-byte units
 // per row. Quad q = half*4 + i of unit u holds the four elements that word i's low (half 0) or high
-// (half 1) nibbles multiply, each pre-scaled by pos_scale(half, jj). Lanes that work on consecutive units
-// read consecutive 16-byte quads, so these loads are free of bank conflicts.
+// (half 1) nibbles multiply, each pre-scaled for its code position (stage_block4). Lanes that work on
+// consecutive units read consecutive 16-byte quads, so these loads are free of bank conflicts.
 __host__ __device__ __forceinline__ uint32_t xs_index(uint32_t v, uint32_t q, uint32_t u, uint32_t U) {
     return ((v * 8u + q) * U + u) * 4u;
-}
-
-// Q4 planar block: element k -> (unit, quad, jj).
-__device__ __forceinline__ void q4_elem_place(uint32_t k, uint32_t& u, uint32_t& q, uint32_t& jj, int& hi) {
-    u = k >> 5;
-    const uint32_t j = k & 31u;
-    hi = (int)(j >> 4);
-    q = (uint32_t)hi * 4u + ((j & 15u) >> 2);
-    jj = j & 3u;
-}
-
-// Q4_K super-block: element k -> (unit, quad, jj). Chunk c = e/64 holds sub-block 2c in the low nibbles
-// of its 32 bytes and sub-block 2c+1 in the high nibbles; unit = 8*sb + 2c + (byte/16).
-__device__ __forceinline__ void q4k_elem_place(uint32_t k, uint32_t& u, uint32_t& q, uint32_t& jj, int& hi) {
-    const uint32_t sb = k >> 8;
-    const uint32_t e = k & 255u;
-    const uint32_t c = e >> 6;
-    const uint32_t t = e & 63u;
-    hi = (int)(t >> 5);
-    const uint32_t byte = t & 31u;
-    u = sb * 8u + c * 2u + (byte >> 4);
-    q = (uint32_t)hi * 4u + ((byte & 15u) >> 2);
-    jj = byte & 3u;
-}
-
-__device__ __forceinline__ float pos_scale_dev(int hi, uint32_t jj) {
-    // the positions of kPosLo / kPosHi packed 5 bits apiece
-    constexpr uint32_t lo = 0u | (8u << 5) | (16u << 10) | (12u << 15);
-    constexpr uint32_t hi_tab = 4u | (12u << 5) | (8u << 10) | (16u << 15);
-    const int p = (int)(((hi ? hi_tab : lo) >> (5u * jj)) & 31u);
-    return __int_as_float((127 + 23 - p) << 23);
 }
 
 // ------------------------------------------------------------------------------------------------

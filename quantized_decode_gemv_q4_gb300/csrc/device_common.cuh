@@ -207,6 +207,28 @@ __device__ __forceinline__ float q4_block_bias(const float4 (&xq)[8], float f) {
     return -((a.x + a.y) * f);
 }
 
+// (n / d, n % d) for n = n0, n0 + step, n0 + 2 * step, ... (all >= 0, d > 0) with two divisions at the start and
+// none per step: the staging loops walk their block indices this way, since a 32-bit division per item costs more
+// than the item's own staging arithmetic.
+struct DivWalk {
+    int q, r;
+    int dq, dr, d;
+    __device__ __forceinline__ DivWalk(int n0, int step, int d_) : d(d_) {
+        q = n0 / d;
+        r = n0 - q * d;
+        dq = step / d;
+        dr = step - dq * d;
+    }
+    __device__ __forceinline__ void next() {
+        q += dq;
+        r += dr;
+        if (r >= d) {
+            r -= d;
+            ++q;
+        }
+    }
+};
+
 // 2^k for -126 <= k <= 127.
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
 
@@ -224,36 +246,52 @@ __device__ __forceinline__ int block_exponent(float m) {
 __device__ __forceinline__ float block_factor(int e) { return 22 + e <= 127 ? pow2i(22 + e) : INFINITY; }
 
 // Four lanes stage one 32-element block: lane t of an aligned group of 4 holds float4 2t and 2t+1 (both in
-// the same half: elements 8t .. 8t+7). The group's sum and largest magnitude (fixed tree), then every lane
-// scales its eight elements with the block's exponent bound e for code positions (hi, jj): the staged value
-// is x * 2^(127-p-e), applied as two exact power-of-two factors per position.
+// the same half: elements 8t .. 8t+7). The group's largest magnitude (fixed tree), then every lane scales its
+// eight elements with the block's exponent bound e for code positions (hi, jj): the staged value is
+// x * 2^(127-p-e), applied as two exact power-of-two factors per position. stage_blocks4 stages NB blocks per
+// group at once, in place: each block takes the same operations in the same order as alone, with the steps of the
+// NB blocks interleaved so that their group shuffles overlap instead of running one block after another.
+template <int NB>
+__device__ __forceinline__ void stage_blocks4(float4 (&a)[NB], float4 (&b)[NB], int hi, int (&e)[NB]) {
+    float m[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+        m[j] = fmaxf(fmaxf(fmaxf(fabsf(a[j].x), fabsf(a[j].y)), fmaxf(fabsf(a[j].z), fabsf(a[j].w))),
+                     fmaxf(fmaxf(fabsf(b[j].x), fabsf(b[j].y)), fmaxf(fabsf(b[j].z), fabsf(b[j].w))));
+#pragma unroll
+    for (int j = 0; j < NB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 1));
+#pragma unroll
+    for (int j = 0; j < NB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 2));
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        e[j] = block_exponent(m[j]);
+        float f1[4], f2[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int p = hi ? (jj == 0 ? 4 : jj == 1 ? 12 : jj == 2 ? 8 : 16) : (jj == 0 ? 0 : jj == 1 ? 8 : jj == 2 ? 16 : 12);
+            const int k = 127 - p - e[j];
+            const int k1 = k >> 1;
+            f1[jj] = pow2i(k1);
+            f2[jj] = pow2i(k - k1);
+        }
+        a[j] = make_float4((a[j].x * f1[0]) * f2[0], (a[j].y * f1[1]) * f2[1], (a[j].z * f1[2]) * f2[2],
+                           (a[j].w * f1[3]) * f2[3]);
+        b[j] = make_float4((b[j].x * f1[0]) * f2[0], (b[j].y * f1[1]) * f2[1], (b[j].z * f1[2]) * f2[2],
+                           (b[j].w * f1[3]) * f2[3]);
+    }
+}
 struct Stage4 {
-    float sum;  // block sum (every lane of the group)
-    int e;      // exponent bound
+    int e;        // exponent bound
     float4 a, b;  // the lane's two float4, scaled
 };
 __device__ __forceinline__ Stage4 stage_block4(float4 a, float4 b, int hi) {
+    float4 aa[1] = {a}, bb[1] = {b};
+    int e[1];
+    stage_blocks4<1>(aa, bb, hi, e);
     Stage4 st;
-    float s = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-    float m = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                    fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    st.sum = s;
-    st.e = block_exponent(m);
-    float f1[4], f2[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const int p = hi ? (jj == 0 ? 4 : jj == 1 ? 12 : jj == 2 ? 8 : 16) : (jj == 0 ? 0 : jj == 1 ? 8 : jj == 2 ? 16 : 12);
-        const int k = 127 - p - st.e;
-        const int k1 = k >> 1;
-        f1[jj] = pow2i(k1);
-        f2[jj] = pow2i(k - k1);
-    }
-    st.a = make_float4((a.x * f1[0]) * f2[0], (a.y * f1[1]) * f2[1], (a.z * f1[2]) * f2[2], (a.w * f1[3]) * f2[3]);
-    st.b = make_float4((b.x * f1[0]) * f2[0], (b.y * f1[1]) * f2[1], (b.z * f1[2]) * f2[2], (b.w * f1[3]) * f2[3]);
+    st.e = e[0];
+    st.a = aa[0];
+    st.b = bb[0];
     return st;
 }
 

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     grid_launch_dependents();
 
     // Staging of the T inputs by threads t0 .. t0 + cnt - 1 (whole warps): four lanes per 32-element block, lane
-    // t of the group holding quads 2t and 2t+1 (block sum and largest magnitude by two group shuffles). Each
+    // t of the group holding quads 2t and 2t+1 (largest magnitude by two group shuffles). Each
     // thread issues the loads of up to kBatch of its block quarters before using any, so staging costs one round
     // trip to the L2 per kBatch quarters.
     constexpr int kBatch = 12;
@@ -179,15 +179,15 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
                     xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                int ej[kBatch];
+                stage_blocks4<kBatch>(xa, xb, t4 >> 1, ej);  // quarters past the end stage zeros and are not stored
+                DivWalk vu(base >> 2, cnt >> 2, U);            // (token, block) of quarter j's block
 #pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int thr = base + j * cnt;
-                    if (thr >= nthr) break;  // warp-uniform
-                    const int blk = thr >> 2;
-                    const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
+                for (int j = 0; j < kBatch; ++j, vu.next()) {
+                    const int blk = (base + j * cnt) >> 2;
                     if (blk < nb_all) {
-                        const int v = blk / U;
-                        const int u = blk - v * U;
+                        const int v = vu.q;
+                        const int u = vu.r;
                         // XG layout: [group of 32 blocks][token][quad][block in group, then a pad]; otherwise
                         // [token][quad][block] (16 bytes each): the lanes of a warp read consecutive 16-byte pieces
                         const int grp32 = u >> 5, ul = u & 31;
@@ -195,16 +195,16 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                         const uint32_t a0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8 + q0) * kXGRow + ul) * 16
                                                                : ((v * 8 + q0) * U + u) * 16);
                         const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
-                                     "f"(st.a.z), "f"(st.a.w)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(xa[j].x), "f"(xa[j].y),
+                                     "f"(xa[j].z), "f"(xa[j].w)
                                      : "memory");
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(st.b.x),
-                                     "f"(st.b.y), "f"(st.b.z), "f"(st.b.w)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + qstep), "f"(xb[j].x),
+                                     "f"(xb[j].y), "f"(xb[j].z), "f"(xb[j].w)
                                      : "memory");
                         if (t4 == 0)
                             asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + (uint32_t)((XG ? (grp32 * p.T + v) * 32 + ul
                                                                                                     : v * U + u) * 8)),
-                                         "f"(block_factor(st.e)), "f"(0.0f)
+                                         "f"(block_factor(ej[j])), "f"(0.0f)
                                          : "memory");
                     }
                 }
@@ -551,9 +551,10 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     // With the first copies in flight: each block's -8 offset term (the unit chain on codes of 8 over its staged
     // quads) and, in CTA 0, the invalid slots' NaN rows and status bit.
     if constexpr (!PURE) {
-        for (int b = threadIdx.x; b < nb_all; b += kThreads) {
-            const int v = b / U;
-            const int u = b - v * U;
+        DivWalk vu((int)threadIdx.x, kThreads, U);
+        for (int b = threadIdx.x; b < nb_all; b += kThreads, vu.next()) {
+            const int v = vu.q;
+            const int u = vu.r;
             const int grp32 = u >> 5, ul = u & 31;
             const uint32_t q0 = xs + (uint32_t)(XG ? (((grp32 * p.T + v) * 8) * kXGRow + ul) * 16 : ((v * 8) * U + u) * 16);
             const uint32_t qstep = XG ? kXGRow * 16u : (uint32_t)U * 16u;

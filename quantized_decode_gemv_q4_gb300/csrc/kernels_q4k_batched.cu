@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
     {
         const int t4 = lane & 3;
         const int nthr = V * nsub * 4;
-        constexpr int kBatch = 8;
+        constexpr int kBatch = V <= 2 ? 2 : 8;  // two quarters per thread cover two vectors at 512 threads and K <= 4096
         for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
         float4 xa[kBatch], xb[kBatch];
 #pragma unroll
@@ -108,15 +108,19 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
             xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // a thread's quarters all lie in sub-blocks of one parity (kThreads / 4 and nsub are even), so they share
+        // the code half k
+        const int k = (base >> 2) & 1;
+        int ej[kBatch];
+        stage_blocks4<kBatch>(xa, xb, k, ej);  // quarters past the end stage zeros and are not stored
+        DivWalk vs(base >> 2, kThreads >> 2, nsub);  // (vector, sub-block) of quarter jb's sub-block
 #pragma unroll
-        for (int jb = 0; jb < kBatch; ++jb) {
+        for (int jb = 0; jb < kBatch; ++jb, vs.next()) {
             const int thr = base + jb * kThreads;
             if (thr >= nthr) break;  // warp-uniform
-            const int jsv = thr >> 2;  // v * nsub + js
-            const int v = jsv / nsub;
-            const int js = jsv - v * nsub;
-            const int k = js & 1;
-            const Stage4 st = stage_block4(xa[jb], xb[jb], k);
+            const int v = vs.q;
+            const int js = vs.r;
+            const Stage4 st = {ej[jb], xa[jb], xb[jb]};
             const uint32_t u = (uint32_t)(js & ~1) + (uint32_t)(t4 >> 1);
             const uint32_t q0 = (uint32_t)(4 * k + ((2 * t4) & 3));
             const uint32_t a0 = xs + xs_index((uint32_t)v, q0, u, U) * 4u;
@@ -137,8 +141,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
         __syncthreads();
         // S of each unit's two halves: the unit chain on codes of 1 (low pairs over quads 0..3, high over 4..7)
         const Word8s c1 = decode_word_sub(0x11111111u);
-        for (int t = threadIdx.x; t < V * (int)U; t += kThreads) {
-            const uint32_t v = (uint32_t)t / U, u = (uint32_t)t - v * U;
+        DivWalk vu((int)threadIdx.x, kThreads, (int)U);
+        for (int t = threadIdx.x; t < V * (int)U; t += kThreads, vu.next()) {
+            const uint32_t v = (uint32_t)vu.q, u = (uint32_t)vu.r;
             float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

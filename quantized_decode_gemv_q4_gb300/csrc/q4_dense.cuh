@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
         const int nthr = ((nb_all * 4 + 31) & ~31);
         // each thread issues the loads of kBatch block quarters before using any (batches of 8 for the wider
         // inputs, whose staging would otherwise take one L2 round trip per 4 quarters)
-        constexpr int kBatch = V >= 2 ? 8 : kStageU / 2;
+        constexpr int kBatch = V >= 3 ? 8 : V == 2 ? 4 : kStageU / 2;
         for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
             float4 xa[kBatch], xb[kBatch];
 #pragma unroll
@@ -174,34 +174,35 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
                 xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
                 xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            int ej[kBatch];
+            stage_blocks4<kBatch>(xa, xb, t4 >> 1, ej);  // quarters past the end stage zeros and are not stored
+            DivWalk vu(base >> 2, kThreads >> 2, p.nblk);  // (vector, block) of quarter j's block
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int thr = base + j * kThreads;
-                if (thr >= nthr) break;  // warp-uniform
-                const int blk = thr >> 2;
-                const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);
+            for (int j = 0; j < kBatch; ++j, vu.next()) {
+                const int blk = (base + j * kThreads) >> 2;
                 if (blk < nb_all) {
-                    const int v = blk / p.nblk;
-                    const uint32_t u = (uint32_t)(blk - v * p.nblk);
+                    const int v = vu.q;
+                    const uint32_t u = (uint32_t)vu.r;
                     const uint32_t a0 = xs + xs_chunk_offset((uint32_t)v, (uint32_t)(2 * t4), u, (uint32_t)V);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y),
-                                 "f"(st.a.z), "f"(st.a.w)
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(xa[j].x), "f"(xa[j].y),
+                                 "f"(xa[j].z), "f"(xa[j].w)
                                  : "memory");
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + kXRow * 16u), "f"(st.b.x), "f"(st.b.y),
-                                 "f"(st.b.z), "f"(st.b.w)
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + kXRow * 16u), "f"(xb[j].x),
+                                 "f"(xb[j].y), "f"(xb[j].z), "f"(xb[j].w)
                                  : "memory");
                     if (t4 == 0)
                         asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(aux + aux_offset((uint32_t)v, u, (uint32_t)V)),
-                                     "f"(block_factor(st.e)), "f"(0.0f)
+                                     "f"(block_factor(ej[j])), "f"(0.0f)
                                      : "memory");
                 }
             }
         }
         __syncthreads();
         // each block's -8 offset term: the unit chain on codes of 8 over its staged quads
-        for (int b = threadIdx.x; b < nb_all; b += kThreads) {
-            const int v = b / p.nblk;
-            const uint32_t u = (uint32_t)(b - v * p.nblk);
+        DivWalk vu((int)threadIdx.x, kThreads, p.nblk);
+        for (int b = threadIdx.x; b < nb_all; b += kThreads, vu.next()) {
+            const int v = vu.q;
+            const uint32_t u = (uint32_t)vu.r;
             float4 xq[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) xq[q] = lds128f(xs + xs_chunk_offset((uint32_t)v, (uint32_t)q, u, (uint32_t)V));

@@ -121,15 +121,16 @@ __global__ void __launch_bounds__(W * 32, 1) q4_xr_kernel(const XrParams p) {
             xa[j] = in ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
             xb[j] = in ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        int ej[kIter];
+        stage_blocks4<kIter>(xa, xb, t4 >> 1, ej);  // every lane takes part in the shuffles
 #pragma unroll
         for (int j = 0; j < kIter; ++j) {
             const int blk = ((int)threadIdx.x + j * W * 32) >> 2;
-            const Stage4 st = stage_block4(xa[j], xb[j], t4 >> 1);  // every lane takes part in the shuffles
             if (blk < p.nblk) {
                 float4* q = xs + ((blk >> 5) * 8 + 2 * t4) * kXRow + (blk & 31);
-                q[0] = st.a;
-                q[kXRow] = st.b;
-                if (t4 == 0) fs[blk] = block_factor(st.e);
+                q[0] = xa[j];
+                q[kXRow] = xb[j];
+                if (t4 == 0) fs[blk] = block_factor(ej[j]);
             }
         }
         __syncthreads();

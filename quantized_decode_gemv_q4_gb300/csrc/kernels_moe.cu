@@ -67,10 +67,10 @@ struct MoEParams {
 
 // Routing tables in shared memory (route_off), each of ms = T*topk rounded up to 32 entries: slot_ids, rank,
 // owner, ucount, uoffset (ms+1), list, group_ux, group_first, group_cnt, scalars[4] (number of distinct experts,
-// number of groups), then the cumulative job cost gcum[ms+1] (64-bit), the job order of the groups gorder
-// (groups sorted by slot count), the token of each list entry ltok, the expert id of each group group_eid and the
-// first job of each of the CTA's warps and of the next CTA (17 entries).
-__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 2 * (ms + 1) + 2 + 3 * ms + 17; }
+// number of groups) and 3 spare entries, then the job order of the groups gorder (groups sorted by slot count),
+// the token of each list entry ltok, the expert id of each group group_eid and the first job of each of the CTA's
+// warps and of the next CTA (17 entries).
+__host__ __device__ constexpr int route_ints(int ms) { return 9 * ms + 8 + 3 * ms + 17; }
 
 // Relative cost of one job (R rows of one projection, all chunks) serving C routed slots: cost_a + cost_b * C
 // (the decode and the streaming are shared, the FMAs grow with C; fitted to measured times of uniform
@@ -125,8 +125,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     int* group_first = route + 7 * ms + 1;
     int* group_cnt = route + 8 * ms + 1;
     int* scalars = route + 9 * ms + 1;
-    long long* gcum = reinterpret_cast<long long*>(route + 9 * ms + 8);  // 8-byte aligned (ms % 32 == 0)
-    int* gorder = route + 9 * ms + 8 + 2 * (ms + 1) + 2;
+    int* gorder = route + 9 * ms + 8;
     int* ltok = gorder + ms;  // token of each list entry (slot / topk), so stages divide nothing
     int* group_eid = ltok + ms;  // expert id of each group
     int* jr = group_eid + ms;    // job ranges of the CTA's warps: warp w takes [jr[w], jr[w + 1])
@@ -152,6 +151,15 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
     // numbered CTA by CTA own contiguous job ranges of equal estimated cost.
     const int gw = p.deal ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * W + warp;
     const int Wtot = (int)gridDim.x * W;
+
+    // Single-warp routing (at most 64 slots) keeps a 64-bit slot mask per expert in the ring's shared memory, which
+    // no copy reaches before the routing is over; the masks are cleared while the previous kernel finishes.
+    const bool route1 = TK <= 64 && (long long)p.E * 8 <= (long long)W * D * SLOT;
+    unsigned long long* const emask = reinterpret_cast<unsigned long long*>(smem + p.slots_off);
+    if (route1) {
+        for (int e = threadIdx.x; e < p.E; e += kThreads) emask[e] = 0ull;
+        __syncthreads();
+    }
 
     // Routing reads the expert ids and the first weight copies depend on it, so wait for the previous kernel
     // in the stream (it may have written ids, x or the outputs) before anything else.
@@ -212,85 +220,100 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         }
     };
 
-    // Job order of the groups (stable by slot count), then the cumulative cost in that order (each group has
-    // 2 * rgs jobs of cost job_cost(cnt)), then this warp's share of the total cost as a contiguous job range
-    // [j0, j1): groups with more routed slots spread over more warps.
+    // Job order of the groups: stable by slot count (the groups of one slot in index order, then those of two, ...),
+    // so the n_c groups of count c take the positions from N_c on (N_c: the groups of fewer slots). Each group has
+    // NP * rgs jobs of cost job_cost(c), so the cost before class c is B_c = sum over c' < c of
+    // n_c' * NP * rgs * job_cost(c'), and the job where the cost reaches x inside class c is
+    // N_c * NP * rgs + floor((x - B_c) / job_cost(c)): each warp's share of the total cost becomes a contiguous job
+    // range [j0, j1) with no table of cumulative costs and no search (groups with more routed slots spread over
+    // more warps).
     auto order_and_ranges = [&]() {
         const int ngroups = scalars[1];
         const int jobs = ngroups * NP * rgs;
-        int base = 0;
-        for (int c = 1; c <= kMaxC; ++c) {
-            for (int c0 = 0; c0 < ngroups; c0 += 32) {
-                const int gi = c0 + lane;
-                const bool mine = gi < ngroups && group_cnt[gi] == c;
-                const unsigned mb = __ballot_sync(0xffffffffu, mine);
-                if (mine) gorder[base + __popc(mb & ((1u << lane) - 1u))] = gi;
-                base += __popc(mb);
-            }
-        }
-        __syncwarp();
-        long long cb = 0;
-        for (int c0 = 0; c0 < ngroups; c0 += 32) {
-            const int oi = c0 + lane;
-            long long v = oi < ngroups ? (long long)NP * rgs * job_cost(group_cnt[gorder[oi]], PURE, p.cost_a, p.cost_b) : 0LL;
+        const unsigned lt = (1u << lane) - 1u;
+        int n[kMaxC + 1];  // groups per slot count (n[0] unused)
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const long long t = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += t;
-            }
-            if (oi < ngroups) gcum[oi + 1] = cb + v;
-            cb += __shfl_sync(0xffffffffu, v, 31);
+        for (int cc = 0; cc <= kMaxC; ++cc) n[cc] = 0;
+        for (int c0 = 0; c0 < ngroups; c0 += 32) {
+            const int gi = c0 + lane;
+            const int c = gi < ngroups ? group_cnt[gi] : 0;
+#pragma unroll
+            for (int cc = 1; cc <= kMaxC; ++cc) n[cc] += __popc(__ballot_sync(0xffffffffu, c == cc));
         }
-        if (lane == 0) gcum[0] = 0;
-        __syncwarp();
+        int next[kMaxC + 1];  // next free position of each class
+        next[1] = 0;
+#pragma unroll
+        for (int cc = 2; cc <= kMaxC; ++cc) next[cc] = next[cc - 1] + n[cc - 1];
+        for (int c0 = 0; c0 < ngroups; c0 += 32) {
+            const int gi = c0 + lane;
+            const int c = gi < ngroups ? group_cnt[gi] : 0;
+            int pos = 0;
+#pragma unroll
+            for (int cc = 1; cc <= kMaxC; ++cc) {
+                const unsigned b = __ballot_sync(0xffffffffu, c == cc);
+                if (c == cc) pos = next[cc] + __popc(b & lt);
+                next[cc] += __popc(b);
+            }
+            if (gi < ngroups) gorder[pos] = gi;
+        }
         // the first job of each of this CTA's warps and of the next CTA's first warp (range dealing)
         if (!p.deal && lane <= W) {
-            const long long c = floor_div(cb * ((int)blockIdx.x * W + lane), Wtot);
+            long long bc[kMaxC + 2];  // B_c
+            int nc[kMaxC + 2];        // N_c
+            bc[1] = 0;
+            nc[1] = 0;
+#pragma unroll
+            for (int cc = 1; cc <= kMaxC; ++cc) {
+                nc[cc + 1] = nc[cc] + n[cc];
+                bc[cc + 1] = bc[cc] + (long long)n[cc] * NP * rgs * job_cost(cc, PURE, p.cost_a, p.cost_b);
+            }
+            const long long cb = bc[kMaxC + 1];
+            const long long x = floor_div(cb * ((int)blockIdx.x * W + lane), Wtot);
             int j = jobs;
-            if (c < cb) {
-                int lo = 0, hi = ngroups - 1;  // largest g with gcum[g] <= c
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (gcum[mid] <= c) lo = mid;
-                    else hi = mid - 1;
-                }
-                j = lo * NP * rgs + (int)floor_div(c - gcum[lo], job_cost(group_cnt[gorder[lo]], PURE, p.cost_a, p.cost_b));
+            if (x < cb) {
+                // the class holding cost x: the last non-empty class that starts at or before x
+                long long b0 = 0, jc = job_cost(1, PURE, p.cost_a, p.cost_b);
+                int n0 = 0;
+#pragma unroll
+                for (int cc = 2; cc <= kMaxC; ++cc)
+                    if (n[cc] > 0 && bc[cc] <= x) {
+                        b0 = bc[cc];
+                        n0 = nc[cc];
+                        jc = job_cost(cc, PURE, p.cost_a, p.cost_b);
+                    }
+                j = n0 * NP * rgs + (int)floor_div(x - b0, jc);
             }
             jr[lane] = j;
         }
     };
 
     // ---- routing, with the inputs staged beside it --------------------------------------------------
-    if (TK <= 64) {
+    if (route1) {
         // Warp 0 routes alone, two slots per lane (slots lane and lane + 32), while the other warps stage the
-        // inputs. Equal experts within a half are found by match, across the halves by 32 shuffles; an invalid or
-        // absent slot gets a key no other slot has. The tables come out as the general path's.
+        // inputs. Each valid slot sets its bit in its expert's 64-bit slot mask (cleared before the dependency
+        // wait); the mask then gives the slot's first equal slot, its rank among them and, on the first slot, their
+        // count. The tables come out as the general path's.
         if (warp == 0) {
             const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
             const int i0 = lane, i1 = lane + 32;
             const int e0 = i0 < TK ? __ldg(p.ids + i0) : -1;
             const int e1 = i1 < TK ? __ldg(p.ids + i1) : -1;
             const bool v0 = i0 < TK && e0 >= 0 && e0 < p.E, v1 = i1 < TK && e1 >= 0 && e1 < p.E;
-            const int k0 = v0 ? e0 : -1 - i0, k1 = v1 ? e1 : -1 - i1;
-            const unsigned m0 = __match_any_sync(full, k0), m1 = __match_any_sync(full, k1);
-            int c10 = 0, f10 = -1, c01 = 0;  // slot i1's equals among slots 0..31 (count, first); slot i0's among 32..63
-            for (int k = 0; k < 32; ++k) {
-                const int a = __shfl_sync(full, k0, k), b = __shfl_sync(full, k1, k);
-                if (a == k1) {
-                    if (f10 < 0) f10 = k;
-                    ++c10;
-                }
-                if (b == k0) ++c01;
-            }
-            const int rank0 = __popc(m0 & lt), first0 = __ffs(m0) - 1;
-            const int rank1 = c10 + __popc(m1 & lt), first1 = f10 >= 0 ? f10 : 32 + __ffs(m1) - 1;
+            if (v0) atomicOr(emask + e0, 1ull << i0);
+            if (v1) atomicOr(emask + e1, 1ull << i1);
+            __syncwarp();
+            const unsigned long long m0 = v0 ? emask[e0] : 0ull, m1 = v1 ? emask[e1] : 0ull;
+            // the ring's copies overwrite the table once the routing is over
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            const int rank0 = __popcll(m0 & ((1ull << i0) - 1ull)), first0 = v0 ? __ffsll((long long)m0) - 1 : i0;
+            const int rank1 = __popcll(m1 & ((1ull << i1) - 1ull)), first1 = v1 ? __ffsll((long long)m1) - 1 : i1;
             const bool isf0 = v0 && first0 == i0, isf1 = v1 && first1 == i1;
             // distinct experts numbered by first appearance (slots 0..31, then 32..63)
             const unsigned b0 = __ballot_sync(full, isf0), b1 = __ballot_sync(full, isf1);
             const int nux0 = __popc(b0);
             const int uxf0 = __popc(b0 & lt), uxf1 = nux0 + __popc(b1 & lt);  // on first slots
             // each expert's slot count and group count on its first slot, then exclusive prefix sums in that order
-            const int cnt0 = isf0 ? __popc(m0) + c01 : 0, cnt1 = isf1 ? __popc(m1) : 0;
+            const int cnt0 = isf0 ? __popcll(m0) : 0, cnt1 = isf1 ? __popcll(m1) : 0;
             const int ng0 = (cnt0 + kMaxC - 1) / kMaxC, ng1 = (cnt1 + kMaxC - 1) / kMaxC;
             int ic0 = cnt0, ig0 = ng0, ic1 = cnt1, ig1 = ng1;
 #pragma unroll
@@ -322,12 +345,13 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
                     group_cnt[goff1 + gi] = min(kMaxC, cnt1 - gi * kMaxC);
                     group_eid[goff1 + gi] = e1;
                 }
-            // each slot's expert index and list position, from its first slot's lane
-            const int ux0 = __shfl_sync(full, uxf0, first0 & 31);
+            // each slot's expert index (the first slots before its own first slot) and list position (from its first
+            // slot's lane)
+            const unsigned long long fb = (unsigned long long)b0 | ((unsigned long long)b1 << 32);  // first slots
+            const int ux0 = __popcll(fb & ((1ull << first0) - 1ull)), ux1 = __popcll(fb & ((1ull << first1) - 1ull));
             const int uo0 = __shfl_sync(full, uoff0, first0 & 31);
-            const int ux1a = __shfl_sync(full, uxf0, first1 & 31), ux1b = __shfl_sync(full, uxf1, first1 & 31);
             const int uo1a = __shfl_sync(full, uoff0, first1 & 31), uo1b = __shfl_sync(full, uoff1, first1 & 31);
-            const int ux1 = first1 < 32 ? ux1a : ux1b, uo1 = first1 < 32 ? uo1a : uo1b;
+            const int uo1 = first1 < 32 ? uo1a : uo1b;
             if (i0 < TK) {
                 slot_ids[i0] = e0;
                 owner[i0] = v0 ? ux0 : -1;

@@ -36,7 +36,7 @@ def test_moe_full_size_64_experts(oracle_lib):
 
 
 @pytest.mark.parametrize("E,N,K,T,topk", [(8, 40, 512, 3, 4), (5, 7, 96, 2, 5), (16, 130, 1024, 1, 2),
-                                          (64, 33, 256, 64, 8)])
+                                          (64, 33, 256, 64, 8), (5000, 7, 96, 3, 5), (20000, 7, 96, 3, 5)])
 def test_moe_shapes(E, N, K, T, topk, oracle_lib):
     m = synth.make_moe(seed=E + N + K, E=E, N=N, K=K, T=T, topk=topk)
     check(m, m["ids"], E, oracle_lib, f"E{E} N{N} K{K} T{T} k{topk}")
@@ -47,6 +47,13 @@ def test_moe_one_expert_for_every_token(oracle_lib):
     m = synth.make_moe(seed=1, E=6, N=50, K=512, T=11, topk=1)
     ids = np.full((11, 1), 3, np.int32)
     check(m, ids, 6, oracle_lib, "all on expert 3")
+
+
+def test_moe_two_experts_over_all_64_slots(oracle_lib):
+    """64 routed slots on two experts, each with slots in both halves of the 64 (42 and 22 slots: many groups)."""
+    m = synth.make_moe(seed=5, E=64, N=72, K=512, T=8, topk=8)
+    ids = np.where(np.arange(64) % 3 == 0, 60, 3).astype(np.int32).reshape(8, 8)
+    check(m, ids, 64, oracle_lib, "two experts")
 
 
 def test_moe_duplicate_expert_within_a_token(oracle_lib):

@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_q4_kernel(const MoEParams p) {
         Cursor k;
         k.grp = j / (NP * rgs);
         const int rem = j - k.grp * NP * rgs;
-        k.sp = rem / rgs;
+        k.sp = NP == 2 && rem >= rgs ? 1 : 0;  // rem < NP * rgs
         k.rg = rem - k.sp * rgs;
         k.c = 0;
         return k;

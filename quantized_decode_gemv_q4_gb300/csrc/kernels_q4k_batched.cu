@@ -7,16 +7,19 @@
 //
 // Kernel shape (one persistent CTA of W warps per SM), the Q4_K kernel's with V vectors:
 //  * the V vectors are staged once per CTA, each 32-element sub-block with its own exponent bound e_{j,v}
-//    (bias-free decode, device_common.cuh); beside each unit (16 quant bytes: half of sub-block 2c in the low
-//    nibbles, the same half of 2c+1 in the high ones) sit (S_lo, S_hi, f_lo, f_hi): f = 2^(22+e) of the two
-//    sub-blocks and S = f times the unit's FMA chain run on codes of 1 over each half;
+//    (bias-free decode, device_common.cuh), with the two code halves interleaved: quad 2i + g of a unit (16 quant
+//    bytes: half of sub-block 2c in the low nibbles, the same half of 2c+1 in the high ones) holds the inputs of
+//    word i's bytes 2g and 2g+1 as (low, high, low, high), so one packed FMA takes a byte's low code into the .x
+//    lane and its high code into the .y lane of one accumulator; beside each unit sit (S_lo, S_hi, f_lo, f_hi):
+//    f = 2^(22+e) of the two sub-blocks and S = f times the unit's FMA chain run on codes of 1 over each half;
 //  * each warp streams R rows (whole rows when they fit) through its own ring of cp.async slots;
 //  * lane l takes unit l (+32, ...) of every row: chunk c = (l%8)/2, half l%2; the 8 lanes of a super-block
 //    each decode one sub-block's header entry (d*sc_j and dmin*m_j), shared with the group by shuffles;
 //  * per word: one shift + eight ANDs per row, then for each vector two staged-input loads (shared by the R
-//    rows) and four packed FMAs per row into one accumulator per sub-block half; per unit and vector the two
-//    halves fold as fl(d*sc*f * A) - fl(dmin*m * S) with unfused rounded operations, so halves whose weights are all zero
-//    (sc = m = 0, or a constant power-of-two code with d*sc*q = dmin*m) contribute exactly zero;
+//    rows) and four packed FMAs per row into the row's (low half, high half) accumulator pair; per unit and
+//    vector the two halves fold as fl(d*sc*f * A) - fl(dmin*m * S) with unfused rounded operations, so halves
+//    whose weights are all zero (sc = m = 0, or a constant power-of-two code with d*sc*q = dmin*m) contribute
+//    exactly zero;
 //  * the R*V totals are summed over the warp with the transposing shuffle reduction and stored.
 #include <algorithm>
 #include <mutex>
@@ -36,6 +39,28 @@ struct Q4KBParams {
     int CS, S, jobs, slot_bytes;
     uint32_t xs_off, ssum_off, slots_off;
 };
+
+// The 8 codes of a word as (low, high) pairs of its bytes 0..3, at the bit positions of decode_word_sub.
+struct Word4p {
+    float2 b0, b1, b2, b3;
+};
+__device__ __forceinline__ Word4p decode_word_pairs(uint32_t w) {
+    const uint32_t s = w >> 12;
+    Word4p r;
+    r.b0 = make_float2(__uint_as_float(w & 0x0000000Fu), __uint_as_float(w & 0x000000F0u));
+    r.b1 = make_float2(__uint_as_float(w & 0x00000F00u), __uint_as_float(w & 0x0000F000u));
+    r.b2 = make_float2(__uint_as_float(w & 0x000F0000u), __uint_as_float(s & 0x00000F00u));
+    r.b3 = make_float2(__uint_as_float(s & 0x0000F000u), __uint_as_float(s & 0x000F0000u));
+    return r;
+}
+// One word of a unit for one row and vector: quads q0 = (lo0, hi0, lo1, hi1) and q1 = (lo2, hi2, lo3, hi3).
+__device__ __forceinline__ float2 word_fma_pairs(const Word4p& d, float4 q0, float4 q1, float2 a) {
+    a = ffma2(d.b0, make_float2(q0.x, q0.y), a);
+    a = ffma2(d.b1, make_float2(q0.z, q0.w), a);
+    a = ffma2(d.b2, make_float2(q1.x, q1.y), a);
+    a = ffma2(d.b3, make_float2(q1.z, q1.w), a);
+    return a;
+}
 
 __device__ __forceinline__ float byte_as_float_b(uint32_t w, int j) {
     return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + (uint32_t)j)) - 8388608.0f;
@@ -122,13 +147,20 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
             const int js = vs.r;
             const Stage4 st = {ej[jb], xa[jb], xb[jb]};
             const uint32_t u = (uint32_t)(js & ~1) + (uint32_t)(t4 >> 1);
-            const uint32_t q0 = (uint32_t)(4 * k + ((2 * t4) & 3));
-            const uint32_t a0 = xs + xs_index((uint32_t)v, q0, u, U) * 4u;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(st.a.x), "f"(st.a.y), "f"(st.a.z),
-                         "f"(st.a.w)
+            // this quarter holds words i0 and i0 + 1 of unit u in one code half (k); lane ^ 4 holds the same words
+            // in the other half. The low-half lane writes word i0 and the high-half lane word i0 + 1, each as its
+            // two interleaved quads
+            const uint32_t i0 = (uint32_t)((2 * t4) & 3);
+            const float4 send = k ? st.a : st.b;
+            const float4 recv = make_float4(__shfl_xor_sync(0xffffffffu, send.x, 4), __shfl_xor_sync(0xffffffffu, send.y, 4),
+                                            __shfl_xor_sync(0xffffffffu, send.z, 4), __shfl_xor_sync(0xffffffffu, send.w, 4));
+            const float4 lo = k ? recv : st.a, hi = k ? st.b : recv;
+            const uint32_t a0 = xs + xs_index((uint32_t)v, 2u * (i0 + (uint32_t)k), u, U) * 4u;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "f"(lo.x), "f"(hi.x), "f"(lo.y),
+                         "f"(hi.y)
                          : "memory");
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + U * 16u), "f"(st.b.x), "f"(st.b.y),
-                         "f"(st.b.z), "f"(st.b.w)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + U * 16u), "f"(lo.z), "f"(hi.z),
+                         "f"(lo.w), "f"(hi.w)
                          : "memory");
             if (t4 == 0) {
                 // f of sub-block js goes to both units of its chunk (.z for the low sub-block, .w for the high)
@@ -139,24 +171,19 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
         }
         }
         __syncthreads();
-        // S of each unit's two halves: the unit chain on codes of 1 (low pairs over quads 0..3, high over 4..7)
-        const Word8s c1 = decode_word_sub(0x11111111u);
+        // S of each unit's two halves: the unit chain on codes of 1, in the main loop's order (.x low, .y high)
+        const Word4p c1 = decode_word_pairs(0x11111111u);
         DivWalk vu((int)threadIdx.x, kThreads, (int)U);
         for (int t = threadIdx.x; t < V * (int)U; t += kThreads, vu.next()) {
             const uint32_t v = (uint32_t)vu.q, u = (uint32_t)vu.r;
-            float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+            float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 xl = lds128f(xs + xs_index(v, (uint32_t)i, u, U) * 4u);
-                const float4 xh = lds128f(xs + xs_index(v, (uint32_t)(4 + i), u, U) * 4u);
-                a = ffma2(c1.lo01, make_float2(xl.x, xl.y), a);
-                a = ffma2(c1.lo23, make_float2(xl.z, xl.w), a);
-                b = ffma2(c1.hi01, make_float2(xh.x, xh.y), b);
-                b = ffma2(c1.hi23, make_float2(xh.z, xh.w), b);
-            }
+            for (int i = 0; i < 4; ++i)
+                a = word_fma_pairs(c1, lds128f(xs + xs_index(v, (uint32_t)(2 * i), u, U) * 4u),
+                                   lds128f(xs + xs_index(v, (uint32_t)(2 * i + 1), u, U) * 4u), a);
             const uint32_t ua = ssum + ((uint32_t)v * U + u) * 16u;
             const float2 f = lds64f(ua + 8u);
-            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ua), "f"((a.x + a.y) * f.x), "f"((b.x + b.y) * f.y)
+            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(ua), "f"(a.x * f.x), "f"(a.y * f.y)
                          : "memory");
         }
     }
@@ -213,29 +240,21 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
                 mhi[r] = __shfl_sync(0xffffffffu, dmm, gbase + (int)(cpos | 1u));
                 w[r] = lds128(slot + it * 144u + 16u + cpos * 16u);
             }
-            float2 aL[R][V], aH[R][V];
+            float2 acc[R][V];  // (low half, high half) of the unit
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                Word8s d8[R];
+                Word4p d4[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    d8[r] = decode_word_sub(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
+                    d4[r] = decode_word_pairs(i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w);
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const uint32_t xa = xs + (uint32_t)v * vstride + u * 16u;
-                    const float4 xl = lds128f(xa + (uint32_t)i * qstride);
-                    const float4 xh = lds128f(xa + (uint32_t)(4 + i) * qstride);
+                    const float4 q0 = lds128f(xa + (uint32_t)(2 * i) * qstride);
+                    const float4 q1 = lds128f(xa + (uint32_t)(2 * i + 1) * qstride);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        float2 a = i == 0 ? make_float2(0.f, 0.f) : aL[r][v];
-                        float2 b = i == 0 ? make_float2(0.f, 0.f) : aH[r][v];
-                        a = ffma2(d8[r].lo01, make_float2(xl.x, xl.y), a);
-                        a = ffma2(d8[r].lo23, make_float2(xl.z, xl.w), a);
-                        b = ffma2(d8[r].hi01, make_float2(xh.x, xh.y), b);
-                        b = ffma2(d8[r].hi23, make_float2(xh.z, xh.w), b);
-                        aL[r][v] = a;
-                        aH[r][v] = b;
-                    }
+                    for (int r = 0; r < R; ++r)
+                        acc[r][v] = word_fma_pairs(d4[r], q0, q1, i == 0 ? make_float2(0.f, 0.f) : acc[r][v]);
                 }
             }
             if (valid) {
@@ -247,8 +266,8 @@ __global__ void __launch_bounds__(W * 32, 1) q4k_batched_kernel(const Q4KBParams
                     for (int r = 0; r < R; ++r) {
                         // fl(d*sc*f * A) - fl(dmin*m * S) per half (d*sc*f and dmin*m are exact), with scalar
                         // rounded operations that the compiler never fuses into an FMA
-                        const float ul = __fmul_rn(dlo[r] * sf.z, aL[r][v].x + aL[r][v].y);
-                        const float uh = __fmul_rn(dhi[r] * sf.w, aH[r][v].x + aH[r][v].y);
+                        const float ul = __fmul_rn(dlo[r] * sf.z, acc[r][v].x);
+                        const float uh = __fmul_rn(dhi[r] * sf.w, acc[r][v].y);
                         tot[r][v].x = __fadd_rn(tot[r][v].x, __fadd_rn(ul, __fmul_rn(mlo[r], sf.x)));
                         tot[r][v].y = __fadd_rn(tot[r][v].y, __fadd_rn(uh, __fmul_rn(mhi[r], sf.y)));
                     }

@@ -6,9 +6,12 @@
 //   float q * 2^(p-149) exactly (a subnormal). The matching input element is staged pre-scaled by
 //   2^(127-p-e) (e bounds its 32-element block's exponent), so one packed fp32x2 FMA adds q * x * 2^(-22-e)
 //   with one rounding.
-// * The FMA chain of a 32-code unit (word_fma) is the one order every kernel uses, and the planar format's -8
-//   offset is removed with the same chain run on a unit of code 8 (q4_block_bias), so a block whose codes are
-//   all 8 (zero weights) contributes exactly zero.
+// * The FMA chain of a 32-code unit (word_fma) is the one order every planar-format kernel uses, and the
+//   format's -8 offset is removed with the same chain run on a unit of code 8 (q4_block_bias), so a block whose
+//   codes are all 8 (zero weights) contributes exactly zero. The Q4_K kernels keep their own chains, with the
+//   sub-block offsets folded from the same chain run on codes of 1.
+// * Input staging (stage_blocks4): four lanes per 32-element block, the block's largest magnitude by two group
+//   shuffles, each element scaled by two exact powers of two; a thread stages a batch of blocks together.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -307,7 +310,7 @@ __host__ __device__ __forceinline__ uint32_t xs_chunk_offset(uint32_t v, uint32_
 __host__ __device__ __forceinline__ uint32_t xs_chunk_bytes(uint32_t V, uint32_t U) {
     return ((U + 31u) / 32u) * V * 8u * kXRow * 16u;
 }
-// Per-block (2^(22+e), -8 * block sum) pairs in the same order: float2[ceil(U/32)][V][32].
+// Per-block (2^(22+e), -8 offset term) pairs in the same order: float2[ceil(U/32)][V][32].
 __host__ __device__ __forceinline__ uint32_t aux_offset(uint32_t v, uint32_t u, uint32_t V) {
     return ((u >> 5) * V + v) * 256u + (u & 31u) * 8u;
 }

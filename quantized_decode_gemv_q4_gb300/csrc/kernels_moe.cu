@@ -9,9 +9,13 @@
 //  * prologue (every CTA, no host synchronisation): read the T*topk ids, find for each slot the first slot
 //    with the same expert and its rank among the slots of that expert, number the distinct experts in
 //    order of first appearance, and cut each expert's slot list into groups of at most kMaxC slots; slots
-//    with an id outside [0, E) get NaN outputs (written by CTA 0) and raise a status bit;
-//  * jobs are (group, projection, row group of R rows), numbered group-major; each warp owns one contiguous
-//    range of jobs (or jobs dealt round-robin), so it streams whole-row stages of consecutive rows through
+//    with an id outside [0, E) get NaN outputs (written by CTA 0) and raise a status bit. Up to 64 slots, warp
+//    0 does this alone from a 64-bit slot mask per expert (one shared-memory atomic OR per slot) while the
+//    other warps stage the inputs; more slots take a table path run by all threads;
+//  * jobs are (group, projection, row group of R rows), numbered group-major with the groups in order of slot
+//    count; each warp owns one contiguous range of jobs of equal estimated cost, found in closed form from
+//    the number of groups per slot count (or jobs dealt round-robin), so it streams whole-row stages of
+//    consecutive rows through
 //    its own ring of slots (bulk copies on a slot mbarrier, or cp.async for chunked rows) with incremental
 //    control, and each selected expert's bytes are read once per call (once per group when more than kMaxC
 //    slots route to one expert);

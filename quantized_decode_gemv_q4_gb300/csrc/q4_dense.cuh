@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(W * 32, 1) q4_gemv_kernel(const Q4Params p) {
         const int nb_all = V * p.nblk;
         const int t4 = lane & 3;
         const int nthr = ((nb_all * 4 + 31) & ~31);
-        // each thread issues the loads of kBatch block quarters before using any (batches of 8 for the wider
-        // inputs, whose staging would otherwise take one L2 round trip per 4 quarters)
+        // each thread issues the loads of kBatch block quarters before using any (batches sized so that one
+        // batch covers a thread's quarters of 2 to 4 vectors at K = 4096: one L2 round trip), then stages them
+        // together
         constexpr int kBatch = V >= 3 ? 8 : V == 2 ? 4 : kStageU / 2;
         for (int base = threadIdx.x; base < nthr; base += kThreads * kBatch) {
             float4 xa[kBatch], xb[kBatch];

@@ -13,10 +13,11 @@
 //    before use), one shift + eight ANDs per word and packed fp32x2 FMAs, folds each block with its scale, and
 //    the warp sums the lanes; the logits go to the CTA's own shared memory;
 //  * after a cluster barrier, CTA 0 gathers the other CTAs' logits through distributed shared memory; a second
-//    barrier releases them; its warp 0 then takes the softmax over all E logits (max subtracted) and K arg-max
-//    passes over a 64-bit key (the logit's order-preserving bits, a NaN below every other value, then the
-//    complement of the index, so ties go to the lower index); taken experts are marked in per-lane bit masks,
-//    and it writes ids and weights (the logits, when asked, come from every CTA).
+//    barrier releases them; its warp 0 then takes the softmax over all E logits (max subtracted) and the top K
+//    by a 64-bit key (the logit's order-preserving bits, a NaN below every other value, then the complement of
+//    the index, so ties go to the lower index): up to 64 experts by each expert's rank among all keys (one
+//    pass of shuffles), otherwise by K arg-max passes with taken experts marked in per-lane bit masks; it
+//    writes ids and weights (the logits, when asked, come from every CTA).
 #include <algorithm>
 #include <mutex>
 
@@ -186,6 +187,45 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
         for (int e = lane; e < p.E; e += 32) z += expf(lg[e] - mx);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        // The ranking key of expert e: the logit's order-preserving bits (-0 ranks with +0, a NaN below every
+        // other value), then the complement of the index, so equal logits go to the lower index.
+        auto key_of = [&](int e) {
+            const float v = lg[e];
+            const uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);
+            const uint32_t key = v != v ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+            return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+        };
+        if (p.E <= 64) {
+            // Up to 64 experts: lane l holds experts l and l + 32; each expert's rank is the number of larger keys
+            // (all keys differ), and the experts of rank < K are the picks in order. The K weights are summed in
+            // pick order, as the passes below do.
+            const bool h0 = lane < p.E, h1 = lane + 32 < p.E;
+            const unsigned long long k0 = h0 ? key_of(lane) : 0ull, k1 = h1 ? key_of(lane + 32) : 0ull;
+            int r0 = 0, r1 = 0;
+#pragma unroll 8
+            for (int sl = 0; sl < 32; ++sl) {
+                const unsigned long long a = __shfl_sync(0xffffffffu, k0, sl), b = __shfl_sync(0xffffffffu, k1, sl);
+                r0 += (int)(a > k0) + (int)(b > k0);
+                r1 += (int)(a > k1) + (int)(b > k1);
+            }
+            float* const pk = reinterpret_cast<float*>(smem + p.xs_off);  // the staged input is no longer needed
+            const float pw0 = h0 ? expf(lg[lane] - mx) / z : 0.f;
+            const float pw1 = h1 ? expf(lg[lane + 32] - mx) / z : 0.f;
+            if (h0 && r0 < p.topk) {
+                pk[r0] = pw0;
+                p.ids[(size_t)t * p.topk + r0] = lane;
+            }
+            if (h1 && r1 < p.topk) {
+                pk[r1] = pw1;
+                p.ids[(size_t)t * p.topk + r1] = lane + 32;
+            }
+            __syncwarp();
+            float wsum = 0.f;
+            for (int i = 0; i < p.topk; ++i) wsum += pk[i];
+            for (int i = lane; i < p.topk; i += 32)
+                p.weights[(size_t)t * p.topk + i] = p.normalize ? pk[i] / wsum : pk[i];
+            return;
+        }
         // K arg-max passes over the untaken experts: lane l holds experts l + 32 j, taken ones marked in
         // tk[j / 32] bit j % 32 (E <= 4096); topk <= E, so a pass always finds an untaken expert
         uint32_t tk[4] = {0u, 0u, 0u, 0u};
@@ -196,10 +236,7 @@ __global__ void __launch_bounds__(W * 32, 1) moe_router_kernel(const RouterParam
             unsigned long long best = 0ull;
             for (int e = lane, j = 0; e < p.E; e += 32, ++j) {
                 if ((tk[j >> 5] >> (j & 31)) & 1u) continue;
-                const float v = lg[e];
-                const uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);  // -0 ranks with +0
-                const uint32_t key = v != v ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
-                const unsigned long long c = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+                const unsigned long long c = key_of(e);
                 best = c > best ? c : best;
             }
 #pragma unroll
